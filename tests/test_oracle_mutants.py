@@ -1,0 +1,56 @@
+"""Planted mistakes: each mutation of the oracle's source must fail a pin.
+
+The mutation is applied to a copy of the C file, compiled to a temporary
+library and loaded beside the real one; the committed oracle is untouched.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle_pins import PINS
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "kf_oracle.c")
+
+MUTANTS = {
+    "interleaved_head_map": ("h / G, t0, t1", "h % j->hkv, t0, t1"),
+    "dropped_log_l": ("*lse = m + log(l);", "*lse = m;"),
+    "dropped_max_in_lse": ("*lse = m + log(l);", "*lse = log(l);"),
+    "missing_normalisation": ("        o[d] /= l;", "        o[d] /= 1.0;"),
+    "dropped_scale": ("s[i] = scale * dot;", "s[i] = dot;"),
+    "v_slot_off_by_one": ("const uint16_t *v = v_cache + cache_row(blk, t % block_size,",
+                          "const uint16_t *v = v_cache + cache_row(blk, (t + 1) % block_size,"),
+    "logical_block_for_k": ("const uint16_t *k = k_cache + cache_row(blk,",
+                            "const uint16_t *k = k_cache + cache_row(t / block_size,"),
+    "k_v_swapped": ("const uint16_t *v = v_cache + cache_row(", "const uint16_t *v = k_cache + cache_row("),
+    "merge_weight_sign": ("double w = exp(li - M);", "double w = exp(M - li);"),
+    "merge_unnormalised": ("        o[d] /= wsum;", "        o[d] /= 1.0;"),
+    "split_short_by_one": ("int64_t hi = lo + chunk * block_size;", "int64_t hi = lo + chunk * block_size - 1;"),
+    "split_per_request_chunk": ("int64_t n_max = (max_context_len + block_size - 1) / block_size;",
+                                "int64_t n_max = (ctx_len + block_size - 1) / block_size;"),
+    "append_slot_off_by_one": ("int64_t dst = cache_row(blk, p % block_size,",
+                               "int64_t dst = cache_row(blk, (p + 1) % block_size,"),
+    "bf16_widen_wrong_half": ("uint32_t u = ((uint32_t)bits) << 16;", "uint32_t u = ((uint32_t)bits) << 15;"),
+    "score_sign": ("s[i] = scale * dot;", "s[i] = -scale * dot;"),
+    "lse_base2": ("*lse = m + log(l);", "*lse = m + log2(l);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation anchor not found: " + name
+    mutated = src.replace(old, new)
+    path = str(tmp_path / ("m_%s.c" % name))
+    with open(path, "w") as f:
+        f.write(mutated)
+    so = oracle.build(force=True, src=path, out=str(tmp_path / ("libm_%s.so" % name)))
+    lib = oracle.load(so)
+    caught = []
+    for pin in PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError):
+            caught.append(pin.__name__)
+    assert caught, "no pin caught mutation " + name
