@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged-KV decode step on GB300: append, split-KV
+attention, LSE merge, through the C-ABI library.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama8b|longctx|shard4|ragged|tiny]
+
+Prints one JSON line. `value` is KV-read GB/s over all ranks: algorithmic KV
+bytes (sum_b L_b * 2 * Hkv * D * 2) per step divided by the device time of a
+step, inputs resident in HBM, timed with CUDA events between a barrier and a
+synchronize on both sides, max over ranks. `e2e` is the same metric with the
+step's inputs copied from pinned host memory and its result copied back
+inside the timed region. `--impl reference` times the fp64 CPU oracle on this
+machine's host cores on a bounded sample of the same workload.
+
+With N > 1 (torchrun), every rank runs its own copy of the workload on its own
+GPU (independent batches, no data-path collective: weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn KV-read GB/s (% of GB300 HBM peak); µs per batch step"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--decode-kernel", default="tc", choices=["tc", "simt"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def default_steps(workload: str) -> int:
+    # about one second of timed device work per workload (clock samples land in it)
+    return {"tiny": 2000, "llama8b": 4000, "longctx": 800, "shard4": 800, "ragged": 250}.get(workload, 200)
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs, copy kernel)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((ts, float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows[-3:]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
+                "sm_max_mhz": max([r[2] for r in inside]) if inside else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ----------------------------------------------------------------------------
+# profile-derived DRAM traffic of the attention kernel (null if stale)
+# ----------------------------------------------------------------------------
+
+def kernel_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("kf_decode_tc.cu", "kf_internal.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_decode_kf_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, kernel: str, kv_bytes_per_launch: float):
+    path = os.path.join(ROOT, "profiles", "attention_dram_traffic.json")
+    if kernel != "tc" or not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        if rec.get("kernel_source_digest") != kernel_source_digest():
+            return None
+        per = rec.get("per_workload", {}).get(workload)
+        if per is None:
+            return None
+        # scaled to one launch of this run by the KV bytes it processes
+        return per["dram_bytes_per_launch"] * kv_bytes_per_launch / per["kv_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# reference arm and CPU baseline: the fp64 oracle on the host cores
+# ----------------------------------------------------------------------------
+
+def oracle_sample(w, target_s: float):
+    """A bounded sample of workload `w` for the oracle: requests (drawn from
+    the workload's own length distribution) until the estimated CPU time is
+    about `target_s` on this machine's cores."""
+    import numpy as np
+    import oracle
+    from paged_kv_decode_kf_gb300 import workloads as wl
+    lay = wl.plan_layout(w)
+    threads = oracle.default_threads()
+    # rate probe on one short request
+    probe = wl.scaled(w, batch=1, lengths=wl.Fixed((int(min(lay.ctx_before.min(), 4096)),)), name="probe")
+    pi = wl.make_inputs(probe, "cpu")
+    args = (wl.bf16_bits(pi.q), wl.bf16_bits(pi.k_cache), wl.bf16_bits(pi.v_cache), pi.block_tables.numpy(),
+            pi.ctx_after.numpy())
+    t = time.time()
+    oracle.attention(*args, w.scale, threads=threads)
+    dt = max(time.time() - t, 1e-4)
+    tok_per_s = float(pi.ctx_after.sum()) / dt
+    budget = tok_per_s * target_s
+    order = np.random.default_rng(w.seed).permutation(w.batch)
+    chosen, tot = [], 0
+    for b in order:
+        if chosen and tot + lay.ctx_after[b] > budget:
+            break
+        chosen.append(int(b))
+        tot += int(lay.ctx_after[b])
+    lens = tuple(int(lay.ctx_before[b]) for b in chosen)
+    sample = wl.scaled(w, batch=len(lens), lengths=wl.Fixed(lens), name=w.name + "-sample", spare_blocks=0)
+    return sample, threads
+
+
+def run_oracle_step(si, threads):
+    import oracle
+    from paged_kv_decode_kf_gb300 import workloads as wl
+    k2, v2, _ = oracle.append(wl.bf16_bits(si.k_cache), wl.bf16_bits(si.v_cache), wl.bf16_bits(si.k_new),
+                              wl.bf16_bits(si.v_new), si.block_tables.numpy(), si.ctx_before.numpy())
+    return oracle.attention(wl.bf16_bits(si.q), k2, v2, si.block_tables.numpy(), si.ctx_after.numpy(),
+                            si.workload.scale, threads=threads)
+
+
+def cpu_baseline(w, target_s=12.0):
+    from paged_kv_decode_kf_gb300 import workloads as wl
+    sample, threads = oracle_sample(w, target_s)
+    si = wl.make_inputs(sample, "cpu")
+    t = time.time()
+    run_oracle_step(si, threads)
+    dt = time.time() - t
+    kv = si.kv_bytes()
+    return {"value": kv / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d requests of the %s workload (%d tokens, %.2f GB of KV), one append + "
+                      "attention pass in fp64 C over all query heads, %.1f s"
+                      % (sample.batch, w.batch, w.name, int(si.ctx_after.sum()), kv / 1e9, dt)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from paged_kv_decode_kf_gb300 import workloads as wl
+    w = wl.CONFIGS[args.workload]
+    K = args.steps if args.steps is not None else 5
+    W = args.warmup
+    per_step_s = max(1.0, min(10.0, 120.0 / max(1, K + W)))
+    sample, threads = oracle_sample(w, per_step_s)
+    si = wl.make_inputs(sample, "cpu")
+    for _ in range(W):
+        run_oracle_step(si, threads)
+    t = time.time()
+    for _ in range(K):
+        run_oracle_step(si, threads)
+    dt = (time.time() - t) / max(K, 1)
+    kv = si.kv_bytes()
+    value = kv / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": K, "warmup": W, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name + ": " + w.description, "sample_requests": sample.batch,
+                   "sample_kv_bytes": kv},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": "%d of %d requests of %s per step (%.3f GB of KV)"
+                                   % (sample.batch, w.batch, w.name, kv / 1e9)},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    os.environ["KF_DECODE_IMPL"] = args.decode_kernel
+
+    import __graft_entry__ as g
+    g.build()
+    from paged_kv_decode_kf_gb300 import workloads as wl
+    from paged_kv_decode_kf_gb300.step import DecodeStep
+
+    w = wl.CONFIGS[args.workload]
+    K = args.steps if args.steps is not None else default_steps(w.name)
+    W = max(args.warmup, 3)
+    dev = wl.make_inputs(w, "cuda:%d" % local)
+    step = DecodeStep(dev)
+    kv_bytes = dev.kv_bytes()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(W):
+        step.run()
+    torch.cuda.synchronize()
+
+    # ---- device-timed region ----
+    n_att = len(step.views)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        if step.with_append:
+            step.append()
+        ev[i][0].record(stream)
+        step.attention()
+        ev[i][1].record(stream)
+        step.merge()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t1 = time.time()
+    clk = clocks.stop(t0, t1)
+    ms = start.elapsed_time(end) / K
+    att_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    from paged_kv_decode_kf_gb300 import kf
+    flags = kf.kf_get_device_error()
+    if flags:
+        sys.stderr.write("device error word 0x%x after the timed region\n" % flags)
+        sys.exit(1)
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    value = kv_bytes * world / (ms * 1e-3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()
+        h = {"q": pin(dev.q), "k_new": pin(dev.k_new), "v_new": pin(dev.v_new),
+             "ctx_before": pin(dev.ctx_before), "ctx_after": pin(dev.ctx_after),
+             "block_tables": pin(dev.block_tables)}
+        if w.shards:
+            h["tail_tables"] = pin(dev.tail_tables)
+            h["tail_ctx_before"] = pin(dev.tail_ctx_before)
+            for j, sv in enumerate(dev.shards):
+                h["shard_bt%d" % j] = pin(sv.block_tables)
+                h["shard_ctx%d" % j] = pin(sv.ctx_after)
+        out_h = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+        lse_h = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in h.values())
+        d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+        def upload():
+            dev.q.copy_(h["q"], non_blocking=True)
+            dev.k_new.copy_(h["k_new"], non_blocking=True)
+            dev.v_new.copy_(h["v_new"], non_blocking=True)
+            dev.ctx_before.copy_(h["ctx_before"], non_blocking=True)
+            dev.ctx_after.copy_(h["ctx_after"], non_blocking=True)
+            dev.block_tables.copy_(h["block_tables"], non_blocking=True)
+            if w.shards:
+                dev.tail_tables.copy_(h["tail_tables"], non_blocking=True)
+                dev.tail_ctx_before.copy_(h["tail_ctx_before"], non_blocking=True)
+                for j, sv in enumerate(dev.shards):
+                    sv.block_tables.copy_(h["shard_bt%d" % j], non_blocking=True)
+                    sv.ctx_after.copy_(h["shard_ctx%d" % j], non_blocking=True)
+
+        Ke = max(3, min(K, 400))
+        for _ in range(3):
+            upload(); step.run(); out_h.copy_(step.out, non_blocking=True); lse_h.copy_(step.lse, non_blocking=True)
+            torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        te0 = time.perf_counter()
+        for _ in range(Ke):
+            upload()
+            step.run()
+            out_h.copy_(step.out, non_blocking=True)
+            lse_h.copy_(step.lse, non_blocking=True)
+            torch.cuda.synchronize()
+        te = (time.perf_counter() - te0) / Ke
+        barrier()
+        if world > 1:
+            tt = torch.tensor([te], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            te = float(tt.item())
+        e2e = {"value": kv_bytes * world / te / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3, "steps": Ke}
+
+    peak, peak_src = hbm_peak()
+    att_gbs = kv_bytes / (att_ms * 1e-3) / 1e9
+    per_launch_kv = kv_bytes / n_att
+    traffic = profiled_traffic(w.name, args.decode_kernel, per_launch_kv)
+    roofline = {"bound": "hbm", "achieved": att_gbs, "peak": peak, "unit": "GB/s", "frac": att_gbs / peak,
+                "traffic": traffic, "kernel": "decode attention (%s)" % args.decode_kernel,
+                "launches_per_step": n_att, "algorithmic_bytes_per_launch": per_launch_kv,
+                "avg_launch_us": att_ms * 1e3 / n_att, "peak_source": peak_src + ", of measured"
+                if peak_src.startswith("measured") else peak_src + ", of fallback"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": ms, "us_per_step": ms * 1e3, "pct_of_hbm_peak": 100.0 * value / world / peak,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "accumulate": "f32", "data": "synthetic",
+            "config": {"workload": w.name + ": " + w.description, "batch": w.batch,
+                       "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                       "block_size": w.block_size, "num_splits": step.num_splits,
+                       "kv_bytes_per_step": kv_bytes, "decode_kernel": args.decode_kernel,
+                       "step": "append + split attention + LSE merge",
+                       "l2": "no flush: the %.2f GB of KV read per step exceeds the 129 MB L2" % (kv_bytes / 1e9)
+                       if kv_bytes > L2_BYTES else "KV fits in L2 (launch-bound case)",
+                       "parallelism": "replica per GPU" if world > 1 else "1 GPU"},
+            "roofline": roofline,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clk,
+            "gpu_launches": K * step.launches_per_step,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

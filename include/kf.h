@@ -1,0 +1,216 @@
+/*
+ * kf.h -- C ABI of the GB300 (sm_103a) split-KV paged decode attention library.
+ *
+ * The operation: one decode step of attention for a batch of requests, each
+ * with one new query token, over a paged KV cache read through a block
+ * table, in split-KV form: a request's tokens are cut into ranges, each range
+ * yields a partial (o, lse), and the partials are combined by an exact
+ * log-sum-exp merge.
+ *
+ * Sources (pages this library restates):
+ *  - KernelFlume (academ.us/article/2606.29207), section 3.1 "Kernel-level
+ *    Disaggregation" and 3.2 "Workflow of Elastic Decoding": attention nodes
+ *    own token-range partitions of the KV cache; the tail node appends the
+ *    step's K_new/V_new, then every node computes local attention and returns
+ *    partials (o_i, m_i, l_i), which are merged by the online-softmax (LSE)
+ *    reduction; section 5.1: the merge equals attention over the full range.
+ *  - "Disaggregated Inference Architecture: Paged KV-Cache Tiering, Chunked
+ *    Prefill, and Asynchronous Overlap" (ultrainstinct.tech), "Physical Memory
+ *    Block Layout" (blocks of block_size tokens x H_KV x D, a block table from
+ *    logical to physical blocks) and "Mathematical Formulation of Chunked
+ *    Attention" (the m/l/O merge update).
+ *  - "The signature-dish specialist: vLLM's attention backend" (blog.lo0.es),
+ *    "How the backend reads the paged KV": the decode kernel gathers the
+ *    physical blocks named by the block table; decode is bound by HBM
+ *    bandwidth ("Why prefill and decode are opposite problems").
+ *
+ * Conventions for every call:
+ *  - Memory: every pointer is DEVICE memory owned by the caller, 16-byte
+ *    aligned, densely packed in the layout stated. The library never
+ *    allocates per call and keeps no per-call state.
+ *  - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and the call returns without synchronising.
+ *  - Host errors: arguments that can be checked on the host are checked
+ *    before anything is launched; a failing check returns KF_ERR_INVALID or
+ *    KF_ERR_UNSUPPORTED and launches nothing. A failed launch returns
+ *    KF_ERR_CUDA.
+ *  - Device errors: values only the GPU sees (block-table entries, context
+ *    lengths) are checked by the kernels. A bad value never causes an
+ *    out-of-bounds access: the access is redirected or skipped, the output
+ *    for that request is unspecified, and a bit is OR-ed into the current
+ *    device's error word, read and cleared by kf_get_device_error().
+ *  - Threads: calls may come from any host thread; the device error word is
+ *    the only state shared between calls.
+ *  - Layouts (bf16 = 16-bit brain float, f32 = IEEE single):
+ *      q            bf16 [batch, num_q_heads, head_dim]
+ *      k_cache      bf16 [num_blocks, block_size, num_kv_heads, head_dim]
+ *      v_cache      bf16 [num_blocks, block_size, num_kv_heads, head_dim]
+ *      block_tables int32 [batch, bt_stride]; entry (b, i) = physical block
+ *                   holding tokens [i*block_size, (i+1)*block_size) of request b
+ *      out_partial  f32 [num_splits, batch, num_q_heads, head_dim]
+ *      lse_partial  f32 [num_splits, batch, num_q_heads]
+ *    Query head h attends with KV head h / (num_q_heads / num_kv_heads).
+ *  - Supported shapes: head_dim 64 or 128; block_size 16 or 32;
+ *    num_q_heads / num_kv_heads in {1, 2, 4, 8}.
+ */
+#ifndef KF_H
+#define KF_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *kf_stream_t;
+
+typedef enum {
+    KF_OK = 0,
+    KF_ERR_INVALID = 1,     /* an argument failed a host-side check; nothing launched */
+    KF_ERR_UNSUPPORTED = 2, /* valid but unsupported shape; nothing launched */
+    KF_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
+    KF_ERR_DEVICE = 4       /* kf_get_device_error: a kernel recorded an error */
+} kf_status;
+
+typedef enum { KF_BF16 = 0, KF_F32 = 1 } kf_dtype;
+
+/* Bits of the device error word. */
+#define KF_DEVERR_BLOCK_ID    0x01u /* a block-table entry outside [0, num_blocks) */
+#define KF_DEVERR_CONTEXT_LEN 0x02u /* a context length < 0 or above bt_stride*block_size */
+#define KF_DEVERR_MAX_CONTEXT 0x04u /* a context length above max_context_len */
+#define KF_DEVERR_APPEND_POS  0x08u /* an append position outside the block table */
+#define KF_DEVERR_TIMEOUT     0x10u /* a pipeline wait in a kernel gave up */
+
+/*
+ * kf_append_kv -- write the step's new K/V row of every request into the cache.
+ *
+ * KernelFlume section 3.2: the tail attention node appends (K_new, V_new)
+ * and then attends over the updated range. For each request b the new token
+ * goes to position p = context_lens_before[b]: physical block
+ * block_tables[b][p / block_size], slot p % block_size, all KV heads. The
+ * copy is bit-exact; no other byte of the caches is written.
+ *
+ *   k_new, v_new         bf16 [batch, num_kv_heads, head_dim]
+ *   k_cache, v_cache     bf16 [num_blocks, block_size, num_kv_heads, head_dim] (written)
+ *   block_tables         int32 [batch, bt_stride]
+ *   context_lens_before  int32 [batch], tokens cached before this step (not modified)
+ *
+ * Device errors: p outside [0, bt_stride*block_size) -> KF_DEVERR_APPEND_POS;
+ * a block id outside [0, num_blocks) -> KF_DEVERR_BLOCK_ID; that request's row
+ * is not written. batch == 0 is a no-op.
+ */
+kf_status kf_append_kv(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                       const int32_t *block_tables, int bt_stride,
+                       const int32_t *context_lens_before, int batch, int num_kv_heads,
+                       int head_dim, int block_size, int64_t num_blocks, kf_stream_t stream);
+
+/*
+ * kf_paged_decode_attention -- split-KV decode attention producing partials.
+ *
+ * KernelFlume sections 3.1-3.2 and 5.1 (local attention over a token range,
+ * returning (o, m, l)); ultrainstinct.tech "Mathematical Formulation of
+ * Chunked Attention". For request b with L_b = context_lens[b] tokens,
+ * query head h (KV head h / G), and split s:
+ *   n_max = ceil(max_context_len / block_size), c = max(1, ceil(n_max / num_splits)),
+ *   the split covers tokens [s*c*block_size, min((s+1)*c*block_size, L_b)),
+ *   s_t = scale * <q[b,h,:], K_t>,  m = max s_t,  l = sum_t e^{s_t - m},
+ *   out_partial[s,b,h,:] = sum_t e^{s_t - m} V_t / l,  lse_partial[s,b,h] = m + ln l.
+ * A split with no tokens writes out_partial = 0 and lse_partial = -inf.
+ * Accumulation is fp32; K/V/q are read as bf16.
+ *
+ *   context_lens     int32 [batch], tokens to attend over (after any append);
+ *                    0 is allowed (every split empty)
+ *   max_context_len  host-side upper bound of context_lens (sets the chunk c)
+ *   scale            softmax scale, e.g. 1/sqrt(head_dim)
+ *   num_splits       >= 1; see kf_choose_num_splits
+ *
+ * A shard (a token-range partition held under its own block table, as on
+ * KernelFlume's attention nodes) is one call with that shard's table and
+ * shard-local lengths, writing its partials at out_partial + j*batch*num_q_heads*head_dim
+ * and lse_partial + j*batch*num_q_heads; one kf_merge_partials over all slots
+ * then gives the full result.
+ *
+ * Host errors: null pointers, batch < 0, num_splits < 1, bt_stride < 1,
+ * num_blocks < 1, max_context_len < 0, a non-finite scale -> KF_ERR_INVALID;
+ * unsupported head_dim, block_size or group -> KF_ERR_UNSUPPORTED.
+ * Device errors: KF_DEVERR_BLOCK_ID, KF_DEVERR_CONTEXT_LEN, KF_DEVERR_MAX_CONTEXT
+ * (tokens beyond the last split are then not attended).
+ */
+kf_status kf_paged_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_tables, int bt_stride,
+                                    const int32_t *context_lens, int max_context_len, int batch,
+                                    int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int64_t num_blocks, float scale,
+                                    int num_splits, float *out_partial, float *lse_partial,
+                                    kf_stream_t stream);
+
+/*
+ * kf_choose_num_splits -- the split count the library would pick for a batch.
+ *
+ * A host-side plan (no device work): it models the decode kernel's schedule
+ * on `device` (SM count, resident work units) and returns the num_splits in
+ * [1, 1024] with the lowest modelled time of attention plus merge. If
+ * context_lens_host (int32 [batch], host memory, nullable) is given it plans
+ * for those lengths; otherwise it assumes every request has max_context_len
+ * tokens. Returns a value < 1 on invalid arguments or a CUDA error.
+ */
+int kf_choose_num_splits(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int max_context_len, const int32_t *context_lens_host,
+                         int device);
+
+/*
+ * kf_choose_num_splits_for -- the same plan for a GPU with `num_sms` SMs,
+ * without touching any device (for planning on the host ahead of time).
+ * The paged-decode pages give no split rule; this is the library's own
+ * schedule model. Returns a value < 1 on invalid arguments.
+ */
+int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_context_len,
+                             const int32_t *context_lens_host, int num_sms);
+
+/*
+ * kf_merge_partials -- exact LSE merge of partial slots.
+ *
+ * ultrainstinct.tech "Mathematical Formulation of Chunked Attention"
+ * (m_new = max(m_prev, m_cur); l and O rescaled by e^{m - m_new} and
+ * summed), restated for normalised partials: for each (b, h),
+ *   M = max_s lse_s,  w_s = e^{lse_s - M},
+ *   out = sum_s w_s o_s / sum_s w_s,  lse_out = M + ln sum_s w_s.
+ * A partial with lse = -inf has weight 0; if every partial of a row is
+ * -inf, out = 0 and lse_out = -inf. KernelFlume section 5.1: the merge of
+ * partials over a partition of the tokens equals attention over all of them.
+ *
+ *   out_partial  f32 [num_partials, batch, num_q_heads, head_dim]
+ *   lse_partial  f32 [num_partials, batch, num_q_heads]
+ *   out          [batch, num_q_heads, head_dim] of out_dtype (bf16 is
+ *                rounded to nearest even)
+ *   lse_out      f32 [batch, num_q_heads], or NULL
+ *
+ * Host errors: null pointers, num_partials < 1, batch < 0, num_q_heads < 1,
+ * bad out_dtype -> KF_ERR_INVALID; head_dim not 64 or 128 -> KF_ERR_UNSUPPORTED.
+ */
+kf_status kf_merge_partials(const float *out_partial, const float *lse_partial,
+                            int num_partials, int batch, int num_q_heads, int head_dim,
+                            void *out, kf_dtype out_dtype, float *lse_out, kf_stream_t stream);
+
+/*
+ * kf_get_device_error -- read and clear the current device's error word.
+ *
+ * Synchronises `stream`, copies the word (KF_DEVERR_* bits) to *flags and
+ * resets it to 0. Returns KF_OK if no bit was set, KF_ERR_DEVICE if some
+ * bit was, KF_ERR_CUDA if a CUDA call failed, KF_ERR_INVALID if flags is NULL.
+ */
+kf_status kf_get_device_error(unsigned int *flags, kf_stream_t stream);
+
+/* Static description of a status code. */
+const char *kf_status_string(kf_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int kf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KF_H */

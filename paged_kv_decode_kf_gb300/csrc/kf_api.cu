@@ -1,0 +1,317 @@
+// kf_api.cu -- the extern "C" surface declared in include/kf.h.
+//
+// Host-side argument checks, the per-device error word, the split planner
+// and dispatch to the kernels. No call allocates device memory: the error
+// word is a __device__ variable of this library (one per device that loads
+// it), and all buffers are the caller's.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <queue>
+#include <vector>
+
+#include "kf_internal.cuh"
+
+namespace kf {
+
+// The device error word (KF_DEVERR_* bits). Host code obtains its device
+// address with cudaGetSymbolAddress, once per device.
+static __device__ unsigned int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    unsigned int *err = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+void *g_encode_fn = nullptr;
+bool g_encode_tried = false;
+
+// Per-device facts, set up on first use with that device current.
+cudaError_t device_info(DeviceInfo **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_error_word);
+        if (e != cudaSuccess) return e;
+        d.ready = true;
+    }
+    *out = &d;
+    return cudaSuccess;
+}
+
+// cuTensorMapEncodeTiled from the driver, without linking libcuda.
+void *encode_fn() {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode_tried) {
+        g_encode_tried = true;
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode_fn = fn;
+    }
+    return g_encode_fn;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_dims(int head_dim, int block_size) {
+    return (head_dim == 64 || head_dim == 128) && (block_size == 16 || block_size == 32);
+}
+
+bool supported_group(int num_q_heads, int num_kv_heads) {
+    if (num_kv_heads < 1 || num_q_heads % num_kv_heads != 0) return false;
+    const int g = num_q_heads / num_kv_heads;
+    return g == 1 || g == 2 || g == 4 || g == 8;
+}
+
+kf_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KF_OK : KF_ERR_CUDA; }
+
+// ----------------------------------------------------------------------------
+// Split planner: a model of the decode kernel's schedule. Work units are
+// (request, KV-head group, split) CTAs launched split-fastest; the hardware
+// hands each free slot the next CTA in launch order, which is simulated with
+// a heap of slot finish times. A CTA with tokens costs a fixed start-up plus
+// its bytes at the per-slot share of HBM bandwidth; an empty one costs its
+// zero-fill. The merge reads and writes S partial rows per output row.
+// ----------------------------------------------------------------------------
+constexpr double kHbmBytesPerUs = 6.0e6;   // sustained HBM bandwidth, bytes per microsecond
+constexpr double kCtaStartUs = 2.0;        // CTA start-up: table, q, first loads in flight
+constexpr double kEmptyCtaUs = 0.25;       // CTA that only writes its empty partial
+constexpr double kLaunchUs = 3.0;          // one kernel launch
+
+double model_time(int S, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                  int block_size, int64_t n_max, const int64_t *n_blocks, int heads_per_cta,
+                  int slots) {
+    const int64_t chunk = std::max<int64_t>(1, (n_max + S - 1) / S);
+    const int groups = (num_kv_heads + heads_per_cta - 1) / heads_per_cta;
+    const double bytes_per_block = 2.0 * block_size * heads_per_cta * head_dim * 2.0;
+    const double slot_bw = kHbmBytesPerUs / slots;
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int i = 0; i < slots; ++i) free_at.push(0.0);
+    double makespan = 0.0;
+    double empty_cost = 0.0;
+    int64_t empties = 0;
+    for (int b = 0; b < batch; ++b) {
+        const int64_t nb = n_blocks ? n_blocks[b] : n_max;
+        for (int g = 0; g < groups; ++g) {
+            for (int s = 0; s < S; ++s) {
+                const int64_t lo = (int64_t)s * chunk;
+                const int64_t cnt = std::max<int64_t>(0, std::min(nb, lo + chunk) - lo);
+                if (cnt == 0) {
+                    ++empties;
+                    continue;
+                }
+                const double t = kCtaStartUs + cnt * bytes_per_block / slot_bw;
+                const double start = free_at.top();
+                free_at.pop();
+                free_at.push(start + t);
+                makespan = std::max(makespan, start + t);
+            }
+        }
+    }
+    empty_cost = empties * kEmptyCtaUs / slots;
+    const double rows = (double)batch * num_q_heads;
+    const double merge_bytes = rows * (S * (head_dim + 1) * 4.0 * 2.0 + head_dim * 4.0);
+    return makespan + empty_cost + kLaunchUs + merge_bytes / kHbmBytesPerUs + kLaunchUs;
+}
+
+}  // namespace
+
+int decode_impl() {
+    // read per call so a process can compare the two kernels
+    const char *s = getenv("KF_DECODE_IMPL");
+    return (s && strcmp(s, "simt") == 0) ? 1 : 0;
+}
+
+}  // namespace kf
+
+using namespace kf;
+
+extern "C" {
+
+const char *kf_status_string(kf_status s) {
+    switch (s) {
+        case KF_OK: return "ok";
+        case KF_ERR_INVALID: return "invalid argument";
+        case KF_ERR_UNSUPPORTED: return "unsupported shape";
+        case KF_ERR_CUDA: return "CUDA error";
+        case KF_ERR_DEVICE: return "a kernel recorded a device error";
+    }
+    return "unknown status";
+}
+
+int kf_version(void) { return 100; }
+
+kf_status kf_append_kv(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                       const int32_t *block_tables, int bt_stride,
+                       const int32_t *context_lens_before, int batch, int num_kv_heads,
+                       int head_dim, int block_size, int64_t num_blocks, kf_stream_t stream) {
+    if (batch < 0 || num_kv_heads < 1 || bt_stride < 1 || num_blocks < 1 || head_dim < 1 ||
+        block_size < 1)
+        return KF_ERR_INVALID;
+    if (batch == 0) return KF_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !block_tables || !context_lens_before)
+        return KF_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return KF_ERR_INVALID;
+    if (!supported_dims(head_dim, block_size)) return KF_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return KF_ERR_CUDA;
+    return from_cuda(launch_append(
+        static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
+        static_cast<uint16_t *>(k_cache), static_cast<uint16_t *>(v_cache), block_tables,
+        bt_stride, context_lens_before, batch, num_kv_heads, head_dim, block_size, num_blocks,
+        dev->err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kf_status kf_paged_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_tables, int bt_stride,
+                                    const int32_t *context_lens, int max_context_len, int batch,
+                                    int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int64_t num_blocks, float scale,
+                                    int num_splits, float *out_partial, float *lse_partial,
+                                    kf_stream_t stream) {
+    if (batch < 0 || num_splits < 1 || bt_stride < 1 || num_blocks < 1 || max_context_len < 0 ||
+        num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || !isfinite(scale))
+        return KF_ERR_INVALID;
+    if (batch == 0) return KF_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out_partial ||
+        !lse_partial)
+        return KF_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out_partial))
+        return KF_ERR_INVALID;
+    if (!supported_dims(head_dim, block_size) || !supported_group(num_q_heads, num_kv_heads))
+        return KF_ERR_UNSUPPORTED;
+    if (batch > 65535 || num_splits > 65535) return KF_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return KF_ERR_CUDA;
+
+    DecodeParams p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.k_cache = static_cast<const uint16_t *>(k_cache);
+    p.v_cache = static_cast<const uint16_t *>(v_cache);
+    p.block_tables = block_tables;
+    p.ctx_lens = context_lens;
+    p.out_partial = out_partial;
+    p.lse_partial = lse_partial;
+    p.err = dev->err;
+    p.num_blocks = num_blocks;
+    p.bt_stride = bt_stride;
+    p.max_context_len = max_context_len;
+    p.batch = batch;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    p.num_splits = num_splits;
+    const int64_t n_max = ((int64_t)max_context_len + block_size - 1) / block_size;
+    p.chunk_blocks = (int)std::max<int64_t>(1, (n_max + num_splits - 1) / num_splits);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (decode_impl() == 1) return from_cuda(launch_decode_simt(p, st));
+    void *fn = encode_fn();
+    if (!fn) return KF_ERR_CUDA;
+    return from_cuda(launch_decode_tc(p, st, fn));
+}
+
+int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_context_len,
+                             const int32_t *context_lens_host, int num_sms) {
+    if (batch < 1 || max_context_len < 0 || num_sms < 1 || block_size < 1 ||
+        !supported_dims(head_dim, block_size) || !supported_group(num_q_heads, num_kv_heads))
+        return -1;
+    const int64_t n_max = ((int64_t)max_context_len + block_size - 1) / block_size;
+    if (n_max <= 1) return 1;
+    std::vector<int64_t> nb;
+    if (context_lens_host) {
+        nb.resize(batch);
+        for (int b = 0; b < batch; ++b) {
+            const int64_t L = std::max<int32_t>(0, context_lens_host[b]);
+            nb[b] = std::min<int64_t>((L + block_size - 1) / block_size, n_max);
+        }
+    }
+    int hpc = 1, cps = 1;
+    if (decode_impl() == 1) {
+        hpc = 1;
+        cps = 8;
+    } else {
+        decode_tc_shape(num_kv_heads, head_dim, block_size, &hpc, &cps);
+    }
+    const int slots = num_sms * cps;
+    static const int cands[] = {1,   2,   3,   4,   5,   6,   7,   8,   10,  12,  14,  16,
+                                20,  24,  28,  32,  40,  48,  56,  64,  80,  96,  112, 128,
+                                160, 192, 224, 256, 320, 384, 448, 512, 640, 768, 896, 1024};
+    int best = 1;
+    double best_t = 1e300;
+    for (int S : cands) {
+        if (S > n_max) break;
+        const double t = model_time(S, batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                    n_max, nb.empty() ? nullptr : nb.data(), hpc, slots);
+        if (t < best_t * 0.995) {  // prefer fewer splits unless clearly faster
+            best_t = t;
+            best = S;
+        }
+    }
+    return best;
+}
+
+int kf_choose_num_splits(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int max_context_len, const int32_t *context_lens_host,
+                         int device) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return -1;
+    return kf_choose_num_splits_for(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                    max_context_len, context_lens_host, sms);
+}
+
+kf_status kf_merge_partials(const float *out_partial, const float *lse_partial,
+                            int num_partials, int batch, int num_q_heads, int head_dim,
+                            void *out, kf_dtype out_dtype, float *lse_out, kf_stream_t stream) {
+    if (num_partials < 1 || batch < 0 || num_q_heads < 1 ||
+        (out_dtype != KF_BF16 && out_dtype != KF_F32))
+        return KF_ERR_INVALID;
+    if (batch == 0) return KF_OK;
+    if (!out_partial || !lse_partial || !out) return KF_ERR_INVALID;
+    if (!aligned16(out_partial) || !aligned16(out)) return KF_ERR_INVALID;
+    if (head_dim != 64 && head_dim != 128) return KF_ERR_UNSUPPORTED;
+    return from_cuda(launch_merge(out_partial, lse_partial, num_partials, batch, num_q_heads,
+                                  head_dim, out, (int)out_dtype, lse_out,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kf_status kf_get_device_error(unsigned int *flags, kf_stream_t stream) {
+    if (!flags) return KF_ERR_INVALID;
+    DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return KF_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    unsigned int word = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KF_ERR_CUDA;
+    if (cudaMemcpy(&word, dev->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KF_ERR_CUDA;
+    if (word != 0 && cudaMemset(dev->err, 0, sizeof word) != cudaSuccess) return KF_ERR_CUDA;
+    *flags = word;
+    return word ? KF_ERR_DEVICE : KF_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,101 @@
+// kf_internal.cuh -- declarations shared by the library's translation units.
+//
+// Internal only: the public surface is include/kf.h. Everything here is
+// device-side helpers and the launch functions the C-ABI layer calls after
+// it has validated the arguments on the host.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kf.h"
+
+namespace kf {
+
+// Parameters of one decode-attention launch (already validated).
+struct DecodeParams {
+    const uint16_t *q;        // bf16 [B, Hq, D]
+    const uint16_t *k_cache;  // bf16 [NB, bs, Hkv, D]
+    const uint16_t *v_cache;
+    const int32_t *block_tables;
+    const int32_t *ctx_lens;
+    float *out_partial;       // f32 [S, B, Hq, D]
+    float *lse_partial;       // f32 [S, B, Hq]
+    unsigned int *err;        // device error word
+    int64_t num_blocks;
+    int bt_stride;
+    int max_context_len;
+    int batch, num_q_heads, num_kv_heads, head_dim, block_size;
+    int num_splits;
+    int chunk_blocks;         // blocks per split: max(1, ceil(ceil(max_ctx/bs)/S))
+    float scale_log2;         // scale * log2(e)
+};
+
+// Decode kernels, one per implementation. Each returns the launch status.
+cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream, void *encode_fn);
+// Largest number of resident CTAs per SM and KV heads per CTA the tensor-core
+// kernel uses for this shape (for the split planner).
+void decode_tc_shape(int num_kv_heads, int head_dim, int block_size, int *heads_per_cta,
+                     int *ctas_per_sm);
+
+cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_cache,
+                          uint16_t *v_cache, const int32_t *block_tables, int bt_stride,
+                          const int32_t *ctx_before, int batch, int num_kv_heads, int head_dim,
+                          int block_size, int64_t num_blocks, unsigned int *err,
+                          cudaStream_t stream);
+
+cudaError_t launch_merge(const float *out_partial, const float *lse_partial, int num_partials,
+                         int batch, int num_q_heads, int head_dim, void *out, int out_dtype,
+                         float *lse_out, cudaStream_t stream);
+
+// Which decode kernel a call uses: 0 = tensor-core (default), 1 = CUDA-core.
+int decode_impl();
+
+// --------------------------------------------------------------------------
+// Device helpers
+// --------------------------------------------------------------------------
+
+__device__ __forceinline__ void raise_error(unsigned int *err, unsigned int bit) {
+    atomicOr(err, bit);
+}
+
+// The two bf16 halves of a 32-bit word as fp32 (exact widening).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Validated context length and the token range of split `s`.
+struct SplitRange {
+    int64_t t_begin, t_end;
+};
+
+__device__ __forceinline__ SplitRange split_range(const DecodeParams &p, int b, int s,
+                                                  bool report) {
+    int64_t L = p.ctx_lens[b];
+    const int64_t cap = (int64_t)p.bt_stride * p.block_size;
+    if (L < 0 || L > cap) {
+        if (report) raise_error(p.err, KF_DEVERR_CONTEXT_LEN);
+        L = L < 0 ? 0 : cap;
+    }
+    if (L > p.max_context_len && report) raise_error(p.err, KF_DEVERR_MAX_CONTEXT);
+    const int64_t span = (int64_t)p.chunk_blocks * p.block_size;
+    int64_t lo = (int64_t)s * span;
+    int64_t hi = lo + span;
+    if (lo > L) lo = L;
+    if (hi > L) hi = L;
+    return {lo, hi};
+}
+
+// Physical block of logical block `lb` of request b, redirected to block 0
+// (and reported) if the table entry is out of range.
+__device__ __forceinline__ int64_t physical_block(const DecodeParams &p, int b, int64_t lb) {
+    int64_t phys = p.block_tables[(int64_t)b * p.bt_stride + lb];
+    if (phys < 0 || phys >= p.num_blocks) {
+        raise_error(p.err, KF_DEVERR_BLOCK_ID);
+        phys = 0;
+    }
+    return phys;
+}
+
+}  // namespace kf

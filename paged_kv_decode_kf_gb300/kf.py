@@ -1,0 +1,178 @@
+"""Thin ctypes binding of the C-ABI library (include/kf.h), same names.
+
+Argument marshalling only: every step of the decode path runs in the
+library's CUDA kernels. Tensors must be CUDA tensors in the layouts kf.h
+states; the current torch stream is used unless one is given. Importing this
+module loads ``_lib/libkf.so`` and fails loudly if it has not been built
+(``__graft_entry__.build()``); there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libkf.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("the kf CUDA library is not built (%s missing); run "
+                      "`python -c 'import __graft_entry__ as g; g.build()'`" % LIB_PATH)
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+KF_OK, KF_ERR_INVALID, KF_ERR_UNSUPPORTED, KF_ERR_CUDA, KF_ERR_DEVICE = range(5)
+KF_BF16, KF_F32 = 0, 1
+KF_DEVERR_BLOCK_ID = 0x01
+KF_DEVERR_CONTEXT_LEN = 0x02
+KF_DEVERR_MAX_CONTEXT = 0x04
+KF_DEVERR_APPEND_POS = 0x08
+KF_DEVERR_TIMEOUT = 0x10
+
+_vp, _i32, _i64, _f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+
+_lib.kf_append_kv.restype = _i32
+_lib.kf_append_kv.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i64, _vp]
+_lib.kf_paged_decode_attention.restype = _i32
+_lib.kf_paged_decode_attention.argtypes = [_vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                           _i32, _i32, _i64, _f32, _i32, _vp, _vp, _vp]
+_lib.kf_choose_num_splits.restype = _i32
+_lib.kf_choose_num_splits.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _i32]
+_lib.kf_choose_num_splits_for.restype = _i32
+_lib.kf_choose_num_splits_for.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _i32]
+_lib.kf_merge_partials.restype = _i32
+_lib.kf_merge_partials.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
+_lib.kf_get_device_error.restype = _i32
+_lib.kf_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), _vp]
+_lib.kf_status_string.restype = ctypes.c_char_p
+_lib.kf_status_string.argtypes = [_i32]
+_lib.kf_version.restype = _i32
+_lib.kf_version.argtypes = []
+
+
+class KfError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what, _lib.kf_status_string(status).decode(), status))
+
+
+def raw():
+    """The loaded ctypes library (for callers that pass raw pointers)."""
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != KF_OK:
+        raise KfError(status, what)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> int:
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def kf_version() -> int:
+    return _lib.kf_version()
+
+
+def kf_append_kv(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                 v_cache: torch.Tensor, block_tables: torch.Tensor,
+                 context_lens_before: torch.Tensor, stream=None) -> None:
+    """Write each request's new K/V row at position context_lens_before[b]."""
+    nb, bs, hkv, d = k_cache.shape
+    B = block_tables.shape[0]
+    _check(_lib.kf_append_kv(
+        _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
+        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _dev(context_lens_before, torch.int32, "context_lens_before"), B, hkv, d, bs, nb,
+        _stream(stream)), "kf_append_kv")
+
+
+def kf_choose_num_splits(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                         block_size: int, max_context_len: int, context_lens_host=None,
+                         device: Optional[int] = None, num_sms: Optional[int] = None) -> int:
+    """The library's split count for this batch (host-side plan)."""
+    arr = None
+    ptr = None
+    if context_lens_host is not None:
+        arr = torch.as_tensor(context_lens_host, dtype=torch.int32).cpu().contiguous()
+        ptr = arr.data_ptr()
+    if num_sms is not None:
+        n = _lib.kf_choose_num_splits_for(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                          max_context_len, ptr, num_sms)
+    else:
+        dev = torch.cuda.current_device() if device is None else device
+        n = _lib.kf_choose_num_splits(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                      max_context_len, ptr, dev)
+    if n < 1:
+        raise KfError(KF_ERR_INVALID, "kf_choose_num_splits")
+    return n
+
+
+def kf_paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                              block_tables: torch.Tensor, context_lens: torch.Tensor,
+                              max_context_len: int, scale: float, num_splits: int,
+                              out_partial: Optional[torch.Tensor] = None,
+                              lse_partial: Optional[torch.Tensor] = None,
+                              stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Split-KV decode attention; returns (out_partial [S,B,Hq,D], lse_partial [S,B,Hq])."""
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if out_partial is None:
+        out_partial = torch.empty((num_splits, B, hq, d), dtype=torch.float32, device=q.device)
+    if lse_partial is None:
+        lse_partial = torch.empty((num_splits, B, hq), dtype=torch.float32, device=q.device)
+    _check(_lib.kf_paged_decode_attention(
+        _dev(q, torch.bfloat16, "q"), _dev(k_cache, torch.bfloat16, "k_cache"),
+        _dev(v_cache, torch.bfloat16, "v_cache"), _dev(block_tables, torch.int32, "block_tables"),
+        block_tables.shape[1], _dev(context_lens, torch.int32, "context_lens"), int(max_context_len),
+        B, hq, hkv, d, bs, nb, float(scale), int(num_splits),
+        _dev(out_partial, torch.float32, "out_partial"), _dev(lse_partial, torch.float32, "lse_partial"),
+        _stream(stream)), "kf_paged_decode_attention")
+    return out_partial, lse_partial
+
+
+def kf_merge_partials(out_partial: torch.Tensor, lse_partial: torch.Tensor,
+                      out: Optional[torch.Tensor] = None, out_dtype=torch.float32,
+                      lse_out: Optional[torch.Tensor] = None, want_lse: bool = True,
+                      stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """LSE merge of [S,B,Hq,D]/[S,B,Hq] partials; returns (out [B,Hq,D], lse [B,Hq] or None)."""
+    S, B, hq, d = out_partial.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=out_dtype, device=out_partial.device)
+    code = {torch.float32: KF_F32, torch.bfloat16: KF_BF16}.get(out.dtype)
+    if code is None:
+        raise ValueError("out must be float32 or bfloat16")
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((B, hq), dtype=torch.float32, device=out_partial.device)
+    _check(_lib.kf_merge_partials(
+        _dev(out_partial, torch.float32, "out_partial"), _dev(lse_partial, torch.float32, "lse_partial"),
+        S, B, hq, d, _dev(out, out.dtype, "out"), code,
+        None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
+        "kf_merge_partials")
+    return out, lse_out
+
+
+def kf_get_device_error(stream=None) -> int:
+    """Synchronise the stream, return and clear the device error word (0 = none)."""
+    flags = ctypes.c_uint(0)
+    st = _lib.kf_get_device_error(ctypes.byref(flags), _stream(stream))
+    if st not in (KF_OK, KF_ERR_DEVICE):
+        raise KfError(st, "kf_get_device_error")
+    return flags.value

@@ -1,0 +1,73 @@
+"""One decode step through the C ABI: append, split attention, merge.
+
+Orchestration of library calls only (buffers come from torch). For a
+workload spread over token-range shards, the append goes through the tail
+table (the shard holding each request's newest position), each shard's
+attention writes its own partial slots, and one merge combines all slots,
+as KernelFlume (academ.us/article/2606.29207) section 3.2 describes for
+attention nodes.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import kf
+from .workloads import DecodeInputs
+
+
+class DecodeStep:
+    def __init__(self, inp: DecodeInputs, num_splits: Optional[int] = None,
+                 out_dtype=torch.float32, with_append: bool = True):
+        self.inp = inp
+        w = inp.workload
+        self.w = w
+        self.with_append = with_append
+        B, Hq, D = w.batch, w.num_q_heads, w.head_dim
+        dev = inp.q.device
+        if w.shards:
+            self.views = [(s.block_tables, s.ctx_after, int(s.ctx_after.max().item())) for s in inp.shards]
+        else:
+            self.views = [(inp.block_tables, inp.ctx_after, inp.max_ctx_after)]
+        if num_splits is None:
+            num_splits = max(self.plan(v[1], v[2]) for v in self.views)
+        self.num_splits = int(num_splits)
+        slots = self.num_splits * len(self.views)
+        self.out_partial = torch.empty((slots, B, Hq, D), dtype=torch.float32, device=dev)
+        self.lse_partial = torch.empty((slots, B, Hq), dtype=torch.float32, device=dev)
+        self.out = torch.empty((B, Hq, D), dtype=out_dtype, device=dev)
+        self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+
+    def plan(self, ctx_lens: torch.Tensor, max_ctx: int) -> int:
+        w = self.w
+        return kf.kf_choose_num_splits(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                       w.block_size, max_ctx, ctx_lens.cpu().numpy().astype(np.int32))
+
+    def append(self, stream=None) -> None:
+        i = self.inp
+        if self.w.shards:
+            kf.kf_append_kv(i.k_new, i.v_new, i.k_cache, i.v_cache, i.tail_tables, i.tail_ctx_before, stream)
+        else:
+            kf.kf_append_kv(i.k_new, i.v_new, i.k_cache, i.v_cache, i.block_tables, i.ctx_before, stream)
+
+    def attention(self, stream=None) -> None:
+        i, S = self.inp, self.num_splits
+        for j, (bt, ctx, max_ctx) in enumerate(self.views):
+            kf.kf_paged_decode_attention(i.q, i.k_cache, i.v_cache, bt, ctx, max_ctx, self.w.scale, S,
+                                         self.out_partial[j * S:(j + 1) * S],
+                                         self.lse_partial[j * S:(j + 1) * S], stream)
+
+    def merge(self, stream=None) -> None:
+        kf.kf_merge_partials(self.out_partial, self.lse_partial, self.out, lse_out=self.lse, stream=stream)
+
+    def run(self, stream=None) -> None:
+        if self.with_append:
+            self.append(stream)
+        self.attention(stream)
+        self.merge(stream)
+
+    @property
+    def launches_per_step(self) -> int:
+        return int(self.with_append) + len(self.views) + 1
