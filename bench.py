@@ -201,14 +201,19 @@ def cpu_baseline(w, target_s=12.0):
     from paged_kv_decode_kf_gb300 import workloads as wl
     sample, threads = oracle_sample(w, target_s)
     si = wl.make_inputs(sample, "cpu")
+    passes = 0
     t = time.time()
-    run_oracle_step(si, threads)
-    dt = time.time() - t
+    while True:                      # repeat the sample until ~target_s of CPU work
+        run_oracle_step(si, threads)
+        passes += 1
+        dt = time.time() - t
+        if dt >= target_s or passes >= 1000:
+            break
     kv = si.kv_bytes()
-    return {"value": kv / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": "%d of %d requests of the %s workload (%d tokens, %.2f GB of KV), one append + "
-                      "attention pass in fp64 C over all query heads, %.1f s"
-                      % (sample.batch, w.batch, w.name, int(si.ctx_after.sum()), kv / 1e9, dt)}
+    return {"value": kv * passes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "%d of %d requests of the %s workload (%d tokens, %.2f GB of KV); %d append + "
+                      "attention passes in fp64 C over all query heads, %.1f s"
+                      % (sample.batch, w.batch, w.name, int(si.ctx_after.sum()), kv / 1e9, passes, dt)}
 
 
 def run_reference(args):

@@ -48,7 +48,7 @@ def test_tiny_workload(kf, impl, S):
     w = wl.CONFIGS["tiny"]
     host = wl.make_inputs(w, "cpu")
     dev = host.to("cuda")
-    hv = _host_all(dev)
+    q, bt, ctx = wl.bf16_bits(host.q), host.block_tables.numpy(), host.ctx_after.numpy()
     with decode_impl(impl):
         kf.kf_append_kv(dev.k_new, dev.v_new, dev.k_cache, dev.v_cache, dev.block_tables, dev.ctx_before)
         o_p, l_p = kf.kf_paged_decode_attention(dev.q, dev.k_cache, dev.v_cache, dev.block_tables,
@@ -60,10 +60,9 @@ def test_tiny_workload(kf, impl, S):
                               host.block_tables.numpy(), host.ctx_before.numpy())
     assert np.array_equal(wl.bf16_bits(dev.k_cache), k2)
     assert np.array_equal(wl.bf16_bits(dev.v_cache), v2)
-    ref_po, ref_pl = oracle.decode_partials(hv.q, k2, v2, hv.tables[0], hv.ctx_after, w.scale, S,
-                                            max_context_len=dev.max_ctx_after)
+    ref_po, ref_pl = oracle.decode_partials(q, k2, v2, bt, ctx, w.scale, S, max_context_len=dev.max_ctx_after)
     check_partials(o_p.cpu().numpy(), l_p.cpu().numpy(), ref_po, ref_pl, "tiny partials")
-    ref_o, ref_l = oracle.attention(hv.q, k2, v2, hv.tables[0], hv.ctx_after, w.scale)
+    ref_o, ref_l = oracle.attention(q, k2, v2, bt, ctx, w.scale)
     check_out(out.cpu().numpy(), ref_o, "tiny out")
     check_lse(lse.cpu().numpy(), ref_l, "tiny lse")
     check_out(out16.float().cpu().numpy(), ref_o, "tiny out bf16")
