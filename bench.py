@@ -123,6 +123,28 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
+# cross-rank aggregation (every rank runs its own copy of the workload)
+# ----------------------------------------------------------------------------
+
+def max_over_ranks(x: float) -> float:
+    """The maximum of a per-rank float over all ranks (identity without a
+    process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank: int, world: int, seconds_max: float) -> float:
+    """Weak scaling: all ranks' bytes over the slowest rank's time."""
+    return bytes_per_rank * world / seconds_max / 1e9
+
+
+# ----------------------------------------------------------------------------
 # profile-derived DRAM traffic of the attention kernel (null if stale)
 # ----------------------------------------------------------------------------
 
@@ -315,11 +337,8 @@ def run_ours(args):
     if flags:
         sys.stderr.write("device error word 0x%x after the timed region\n" % flags)
         sys.exit(1)
-    if world > 1:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    value = kv_bytes * world / (ms * 1e-3) / 1e9
+    ms = max_over_ranks(ms)
+    value = whole_job_gbs(kv_bytes, world, ms * 1e-3)
 
     # ---- end to end through the C ABI with host buffers ----
     e2e = None
@@ -368,11 +387,8 @@ def run_ours(args):
             torch.cuda.synchronize()
         te = (time.perf_counter() - te0) / Ke
         barrier()
-        if world > 1:
-            tt = torch.tensor([te], device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            te = float(tt.item())
-        e2e = {"value": kv_bytes * world / te / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        te = max_over_ranks(te)
+        e2e = {"value": whole_job_gbs(kv_bytes, world, te), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3, "steps": Ke}
 
     peak, peak_src = hbm_peak()
