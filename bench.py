@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--decode-kernel", default="tc", choices=["tc", "simt"])
+    ap.add_argument("--path", default="auto", choices=["auto", "fused", "calls"],
+                    help="fused: kf_decode_step (one launch); calls: append, attention, merge; "
+                         "auto: fused for unsharded workloads with the tensor-core kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -158,15 +161,17 @@ def kernel_source_digest() -> str:
 
 
 def profiled_traffic(workload: str, kernel: str, kv_bytes_per_launch: float):
+    """`kernel` is "tc" (attention launch of the three-call path) or "fused"
+    (the single-launch step)."""
     path = os.path.join(ROOT, "profiles", "attention_dram_traffic.json")
-    if kernel != "tc" or not os.path.exists(path):
+    if kernel not in ("tc", "fused") or not os.path.exists(path):
         return None
     try:
         with open(path) as f:
             rec = json.load(f)
         if rec.get("kernel_source_digest") != kernel_source_digest():
             return None
-        per = rec.get("per_workload", {}).get(workload)
+        per = rec.get("per_workload" if kernel == "tc" else "per_workload_fused", {}).get(workload)
         if per is None:
             return None
         # scaled to one launch of this run by the KV bytes it processes
@@ -296,7 +301,8 @@ def run_ours(args):
     K = args.steps if args.steps is not None else default_steps(w.name)
     W = max(args.warmup, 3)
     dev = wl.make_inputs(w, "cuda:%d" % local)
-    step = DecodeStep(dev)
+    fused = args.path == "fused" or (args.path == "auto" and not w.shards and args.decode_kernel == "tc")
+    step = DecodeStep(dev, fused=fused)
     kv_bytes = dev.kv_bytes()
     stream = torch.cuda.current_stream()
 
@@ -319,6 +325,11 @@ def run_ours(args):
     t0 = time.time()
     start.record(stream)
     for i in range(K):
+        if step.fused:
+            ev[i][0].record(stream)
+            step.step_fused()
+            ev[i][1].record(stream)
+            continue
         if step.with_append:
             step.append()
         ev[i][0].record(stream)
@@ -394,9 +405,11 @@ def run_ours(args):
     peak, peak_src = hbm_peak()
     att_gbs = kv_bytes / (att_ms * 1e-3) / 1e9
     per_launch_kv = kv_bytes / n_att
-    traffic = profiled_traffic(w.name, args.decode_kernel, per_launch_kv)
+    traffic = profiled_traffic(w.name, "fused" if step.fused else args.decode_kernel, per_launch_kv)
+    kname = ("decode step, one launch (append + attention + merge)" if step.fused
+             else "decode attention (%s)" % args.decode_kernel)
     roofline = {"bound": "hbm", "achieved": att_gbs, "peak": peak, "unit": "GB/s", "frac": att_gbs / peak,
-                "traffic": traffic, "kernel": "decode attention (%s)" % args.decode_kernel,
+                "traffic": traffic, "kernel": kname,
                 "launches_per_step": n_att, "algorithmic_bytes_per_launch": per_launch_kv,
                 "avg_launch_us": att_ms * 1e3 / n_att, "peak_source": peak_src + ", of measured"
                 if peak_src.startswith("measured") else peak_src + ", of fallback"}
@@ -416,6 +429,8 @@ def run_ours(args):
                        "block_size": w.block_size, "num_splits": step.num_splits,
                        "kv_bytes_per_step": kv_bytes, "decode_kernel": args.decode_kernel,
                        "step": "append + split attention + LSE merge",
+                       "path": "kf_decode_step (one launch)" if step.fused else
+                               "kf_append_kv + kf_paged_decode_attention x%d + kf_merge_partials" % n_att,
                        "l2": "no flush: the %.2f GB of KV read per step exceeds the 129 MB L2" % (kv_bytes / 1e9)
                        if kv_bytes > L2_BYTES else "KV fits in L2 (launch-bound case)",
                        "parallelism": "replica per GPU" if world > 1 else "1 GPU"},

@@ -56,6 +56,7 @@
 #ifndef KF_H
 #define KF_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -193,6 +194,47 @@ int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int h
 kf_status kf_merge_partials(const float *out_partial, const float *lse_partial,
                             int num_partials, int batch, int num_q_heads, int head_dim,
                             void *out, kf_dtype out_dtype, float *lse_out, kf_stream_t stream);
+
+/*
+ * kf_decode_step -- the whole decode step in one kernel launch: append,
+ * split-KV attention and LSE merge.
+ *
+ * Same arithmetic as kf_append_kv, then kf_paged_decode_attention over
+ * context_lens_before[b] + 1 tokens, then kf_merge_partials (KernelFlume
+ * sections 3.2 and 5.1; ultrainstinct.tech "Mathematical Formulation of
+ * Chunked Attention"), with the split rule of kf_paged_decode_attention and
+ * c computed from max_context_len. Differences in what is written: the new
+ * K/V row goes to the cache as in kf_append_kv; splits with no tokens write
+ * nothing; partials of requests with more than one non-empty split live in
+ * `workspace` and are merged there by the last work unit to finish; only
+ * `out` and `lse_out` are results.
+ *
+ *   context_lens_before  int32 [batch], tokens cached before this step (>= 0)
+ *   max_context_len      host-side upper bound of context_lens_before + 1
+ *   workspace            device scratch of kf_decode_step_workspace_size() bytes,
+ *                        16-byte aligned, ZERO-FILLED before its first use; every
+ *                        completed call leaves its counters at zero again. Calls
+ *                        that share a workspace must not overlap on the GPU.
+ *                        May be NULL when num_splits == 1.
+ *   out                  [batch, num_q_heads, head_dim] of out_dtype
+ *   lse_out              f32 [batch, num_q_heads], or NULL
+ *
+ * Host errors as kf_paged_decode_attention, plus: a missing or short workspace
+ * with num_splits > 1 -> KF_ERR_INVALID; num_splits too large for the merge to
+ * fit in the kernel's shared memory -> KF_ERR_UNSUPPORTED.
+ * Device errors: KF_DEVERR_BLOCK_ID, KF_DEVERR_CONTEXT_LEN (negative length),
+ * KF_DEVERR_APPEND_POS (no room in the table), KF_DEVERR_MAX_CONTEXT.
+ */
+size_t kf_decode_step_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                     int num_splits);
+
+kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                         void *v_cache, const int32_t *block_tables, int bt_stride,
+                         const int32_t *context_lens_before, int max_context_len, int batch,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int64_t num_blocks, float scale, int num_splits, void *workspace,
+                         size_t workspace_bytes, void *out, kf_dtype out_dtype, float *lse_out,
+                         kf_stream_t stream);
 
 /*
  * kf_get_device_error -- read and clear the current device's error word.

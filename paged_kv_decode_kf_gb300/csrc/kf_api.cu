@@ -234,6 +234,93 @@ kf_status kf_paged_decode_attention(const void *q, const void *k_cache, const vo
     return from_cuda(launch_decode_tc(p, st, fn));
 }
 
+size_t kf_decode_step_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                     int num_splits) {
+    if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || num_splits < 1) return 0;
+    const size_t rows = (size_t)batch * num_q_heads;
+    const auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    return al((size_t)num_splits * rows * head_dim * 4) + al((size_t)num_splits * rows * 4) +
+           al((size_t)batch * num_kv_heads * 4);
+}
+
+kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                         void *v_cache, const int32_t *block_tables, int bt_stride,
+                         const int32_t *context_lens_before, int max_context_len, int batch,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int64_t num_blocks, float scale, int num_splits, void *workspace,
+                         size_t workspace_bytes, void *out, kf_dtype out_dtype, float *lse_out,
+                         kf_stream_t stream) {
+    if (batch < 0 || num_splits < 1 || bt_stride < 1 || num_blocks < 1 || max_context_len < 0 ||
+        num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || !isfinite(scale) ||
+        (out_dtype != KF_BF16 && out_dtype != KF_F32))
+        return KF_ERR_INVALID;
+    if (batch == 0) return KF_OK;
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !block_tables || !context_lens_before ||
+        !out)
+        return KF_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
+        !aligned16(v_cache) || !aligned16(out))
+        return KF_ERR_INVALID;
+    if (!supported_dims(head_dim, block_size) || !supported_group(num_q_heads, num_kv_heads))
+        return KF_ERR_UNSUPPORTED;
+    if (batch > 65535 || num_splits > 65535) return KF_ERR_UNSUPPORTED;
+    const size_t need = kf_decode_step_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                      num_splits);
+    if (num_splits > 1 && (!workspace || !aligned16(workspace) || workspace_bytes < need))
+        return KF_ERR_INVALID;
+    // the last CTA of a group merges in its shared-memory ring: S x rows x 4 bytes must fit
+    int hpc = 1, cps = 1;
+    decode_tc_shape(num_kv_heads, head_dim, block_size, &hpc, &cps);
+    const int R = hpc * (num_q_heads / num_kv_heads);
+    if ((int64_t)num_splits * R * 4 + 8 * R > decode_tc_ring_bytes(num_kv_heads, head_dim))
+        return KF_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return KF_ERR_CUDA;
+
+    DecodeParams p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.k_cache = static_cast<const uint16_t *>(k_cache);
+    p.v_cache = static_cast<const uint16_t *>(v_cache);
+    p.block_tables = block_tables;
+    p.ctx_lens = context_lens_before;
+    p.out_partial = nullptr;
+    p.lse_partial = nullptr;
+    p.err = dev->err;
+    p.num_blocks = num_blocks;
+    p.bt_stride = bt_stride;
+    p.max_context_len = max_context_len;
+    p.batch = batch;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    p.num_splits = num_splits;
+    const int64_t n_max = ((int64_t)max_context_len + block_size - 1) / block_size;
+    p.chunk_blocks = (int)std::max<int64_t>(1, (n_max + num_splits - 1) / num_splits);
+    p.scale_log2 = scale * 1.4426950408889634f;
+
+    const size_t rows = (size_t)batch * num_q_heads;
+    const auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    StepArgs a;
+    a.k_new = static_cast<const uint16_t *>(k_new);
+    a.v_new = static_cast<const uint16_t *>(v_new);
+    a.k_cache = static_cast<uint16_t *>(k_cache);
+    a.v_cache = static_cast<uint16_t *>(v_cache);
+    a.ws_o = num_splits > 1 ? reinterpret_cast<float *>(ws) : nullptr;
+    a.ws_lse = num_splits > 1 ? reinterpret_cast<float *>(ws + al((size_t)num_splits * rows * head_dim * 4)) : nullptr;
+    a.counters = num_splits > 1 ? reinterpret_cast<unsigned int *>(
+                                      ws + al((size_t)num_splits * rows * head_dim * 4) +
+                                      al((size_t)num_splits * rows * 4))
+                                : nullptr;
+    a.out = out;
+    a.lse_out = lse_out;
+    a.out_dtype = (int)out_dtype;
+    void *fn = encode_fn();
+    if (!fn) return KF_ERR_CUDA;
+    return from_cuda(launch_decode_step_tc(p, a, reinterpret_cast<cudaStream_t>(stream), fn));
+}
+
 int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                              int block_size, int max_context_len,
                              const int32_t *context_lens_host, int num_sms) {

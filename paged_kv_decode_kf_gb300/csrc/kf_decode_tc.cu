@@ -143,6 +143,20 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // ---------------------------------------------------------------------------
 // Kernel
 // ---------------------------------------------------------------------------
+// Extra inputs/outputs of the single-launch decode step.
+struct StepParams {
+    const uint16_t *k_new;   // bf16 [B, Hkv, D]
+    const uint16_t *v_new;
+    uint16_t *k_cache;       // the caches, written at the appended position
+    uint16_t *v_cache;
+    float *ws_o;             // workspace: partials [S, B, Hq, D]
+    float *ws_lse;           //            lse     [S, B, Hq]
+    unsigned int *counters;  //            [B, Hkv], zero between steps
+    void *out;               // final [B, Hq, D] (f32 or bf16)
+    float *lse_out;          // final [B, Hq], or null
+    int out_dtype;
+};
+
 template <int D, int HPC, int NS>
 struct TcShape {
     static constexpr int kHalves = D / 64;                 // 64-element boxes per row
@@ -152,9 +166,82 @@ struct TcShape {
     static constexpr int kThreads = 32 * (HPC + 1);
 };
 
-template <int D, int HPC, int G, int NS>
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Number of splits of a request with L tokens that hold at least one token.
+__device__ __forceinline__ int nonempty_splits(const DecodeParams &p, int64_t L) {
+    const int64_t nb = (L + p.block_size - 1) / p.block_size;
+    int64_t n = (nb + p.chunk_blocks - 1) / p.chunk_blocks;
+    return (int)(n < p.num_splits ? n : p.num_splits);
+}
+
+// Last-arriving CTA of a (request, KV-head group): LSE merge of the n_ne
+// partials in the workspace into the final rows (same arithmetic as the merge
+// kernel). Uses the shared-memory ring, which is idle by now.
+template <int D, int R>
+__device__ void merge_group(const DecodeParams &p, const StepParams &sp, int b, int row_first,
+                            int n_ne, float *sm) {
+    const int64_t rows = (int64_t)p.batch * p.num_q_heads;
+    float *sm_w = sm;                 // [n_ne][R] lse, then weights
+    float *sm_m = sm + n_ne * R;      // [R] row max
+    float *sm_sum = sm_m + R;         // [R] sum of weights
+    const int nt = blockDim.x, tid = threadIdx.x;
+    for (int i = tid; i < n_ne * R; i += nt) {
+        const int s = i / R, r = i % R;
+        sm_w[i] = __ldcg(sp.ws_lse + (int64_t)s * rows + (int64_t)b * p.num_q_heads + row_first + r);
+    }
+    __syncthreads();
+    for (int r = tid; r < R; r += nt) {
+        float M = -INFINITY;
+        for (int s = 0; s < n_ne; ++s) M = fmaxf(M, sm_w[s * R + r]);
+        float sum = 0.f;
+        for (int s = 0; s < n_ne; ++s) {
+            const float w = expf(sm_w[s * R + r] - M);
+            sm_w[s * R + r] = w;
+            sum += w;
+        }
+        sm_m[r] = M;
+        sm_sum[r] = sum;
+    }
+    __syncthreads();
+    constexpr int C = D / 4;
+    for (int u = tid; u < R * C; u += nt) {
+        const int r = u / C, c = u % C;
+        const int64_t row = (int64_t)b * p.num_q_heads + row_first + r;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int s = 0; s < n_ne; ++s) {
+            const float w = sm_w[s * R + r];
+            const float4 o = __ldcg(reinterpret_cast<const float4 *>(sp.ws_o + ((int64_t)s * rows + row) * D) + c);
+            acc.x = fmaf(w, o.x, acc.x);
+            acc.y = fmaf(w, o.y, acc.y);
+            acc.z = fmaf(w, o.z, acc.z);
+            acc.w = fmaf(w, o.w, acc.w);
+        }
+        const float inv = 1.f / sm_sum[r];
+        acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+        if (sp.out_dtype == KF_F32) {
+            reinterpret_cast<float4 *>(static_cast<float *>(sp.out) + row * D)[c] = acc;
+        } else {
+            uint2 v;
+            v.x = pack_bf16(acc.x, acc.y);
+            v.y = pack_bf16(acc.z, acc.w);
+            reinterpret_cast<uint2 *>(static_cast<uint16_t *>(sp.out) + row * D)[c] = v;
+        }
+        if (c == 0 && sp.lse_out) sp.lse_out[row] = sm_m[r] + logf(sm_sum[r]);
+    }
+}
+
+// FUSED = false: one split's partial into out_partial (empty split -> 0, -inf).
+// FUSED = true: the whole decode step. ctx_lens are the pre-append lengths;
+// CTAs of empty splits exit at once; the tail split appends the new K/V row;
+// a request with one non-empty split writes its final rows directly, others
+// go through the workspace and the last CTA merges.
+template <int D, int HPC, int G, int NS, bool FUSED>
 __global__ void __launch_bounds__(TcShape<D, HPC, NS>::kThreads)
-decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
+decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v) {
     using Sh = TcShape<D, HPC, NS>;
     constexpr int KS = D / 16;  // k-steps of Q.K and m-tiles of O^T
@@ -168,10 +255,33 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h0 = hg * HPC;
     const int Hq = p.num_q_heads;
-    const int64_t row0 = ((int64_t)s * p.batch + b) * Hq + (int64_t)h0 * G;  // first output row
+    const bool report = threadIdx.x == 0 && s == 0 && hg == 0;
 
-    const SplitRange r = split_range(p, b, s, threadIdx.x == 0 && s == 0 && hg == 0);
-    if (r.t_begin >= r.t_end || (*(volatile unsigned int *)p.err & KF_DEVERR_TIMEOUT)) {
+    // token range of this split; in the fused step the range covers the new token too
+    int64_t p_new = -1;  // position the step appends (fused only)
+    int n_ne = 0;
+    SplitRange r;
+    if (FUSED) {
+        const int64_t before = p.ctx_lens[b];
+        const int64_t cap = (int64_t)p.bt_stride * p.block_size;
+        int64_t L = before + 1;
+        if (before < 0 || L > cap) {
+            if (report) raise_error(p.err, before < 0 ? KF_DEVERR_CONTEXT_LEN : KF_DEVERR_APPEND_POS);
+            L = before < 0 ? 0 : cap;
+        } else {
+            p_new = before;
+        }
+        if (L > p.max_context_len && report) raise_error(p.err, KF_DEVERR_MAX_CONTEXT);
+        n_ne = nonempty_splits(p, L);
+        if (s >= n_ne) return;  // no tokens: nothing written, not counted
+        const int64_t span = (int64_t)p.chunk_blocks * p.block_size;
+        r.t_begin = (int64_t)s * span;
+        r.t_end = r.t_begin + span < L ? r.t_begin + span : L;
+    } else {
+        r = split_range(p, b, s, report);
+    }
+    const int64_t row0 = ((int64_t)s * p.batch + b) * Hq + (int64_t)h0 * G;  // first partial row
+    if (!FUSED && (r.t_begin >= r.t_end || (*(volatile unsigned int *)p.err & KF_DEVERR_TIMEOUT))) {
         for (int i = threadIdx.x; i < HPC * G * D; i += blockDim.x) p.out_partial[row0 * D + i] = 0.f;
         for (int i = threadIdx.x; i < HPC * G; i += blockDim.x) p.lse_partial[row0 + i] = -INFINITY;
         return;
@@ -188,6 +298,7 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_
     }
     __syncthreads();
 
+    bool ok = true;
     if (warp == HPC) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
@@ -211,151 +322,226 @@ decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_
                 }
             }
         }
-        return;
-    }
+        if (!FUSED) return;
+    } else {
+        // ------------------------------- consumers --------------------------------
+        const int g = lane >> 2, qd = lane & 3;
+        const int hkv = h0 + warp;
+        const int hq = hkv * G;  // first query head of this warp's KV head
 
-    // ------------------------------- consumers --------------------------------
-    const int g = lane >> 2, qd = lane & 3;
-    const int hq = (h0 + warp) * G;  // first query head of this warp's KV head
-
-    // Q^T as B fragments: b0 = Q[g][16ks + 2qd .. +1], b1 = Q[g][16ks + 8 + 2qd .. +1]
-    uint32_t qb[KS][2];
+        // Q^T as B fragments: b0 = Q[g][16ks + 2qd .. +1], b1 = Q[g][16ks + 8 + 2qd .. +1]
+        uint32_t qb[KS][2];
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qb[ks][1] = 0u;
-    if (g < G) {
-        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + ((int64_t)b * Hq + hq + g) * D);
+        for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qb[ks][1] = 0u;
+        if (g < G) {
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + ((int64_t)b * Hq + hq + g) * D);
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            qb[ks][0] = qrow[8 * ks + qd];
-            qb[ks][1] = qrow[8 * ks + 4 + qd];
-        }
-    }
-
-    float oacc[KS][4];
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY};
-    float l_acc[2] = {0.f, 0.f};
-
-    // ldmatrix row addresses: lane -> (matrix j = lane/8, row = lane%8)
-    const int lj = lane >> 3, lr = lane & 7;
-    const uint32_t head_off = warp * (kTok * 128);  // this head's 16 rows in a box
-    bool ok = true;
-
-    for (int i = 0; i < n_sub; ++i) {
-        const int st = i % NS;
-        if (!mbar_wait(bars + 8 * st, (i / NS) & 1)) {
-            raise_error(p.err, KF_DEVERR_TIMEOUT);
-            ok = false;
-            break;
-        }
-        const uint32_t kbuf = base + st * Sh::kStageBytes + head_off;
-        const uint32_t vbuf = kbuf + Sh::kHalves * Sh::kBoxBytes;
-        const int64_t t_base = (sb0 + i) * kTok;
-        const int64_t rem_tok = r.t_end - t_base;
-        const int nvalid = rem_tok < kTok ? (int)rem_tok : kTok;
-
-        if (nvalid < kTok) {
-            // zero this head's V rows past the end (whole 128-byte rows, any swizzle)
-            for (int idx = lane; idx < (kTok - nvalid) * 8 * Sh::kHalves; idx += 32) {
-                const int hf = idx / ((kTok - nvalid) * 8);
-                const int rem = idx % ((kTok - nvalid) * 8);
-                const int t = nvalid + rem / 8, c = rem % 8;
-                const uint32_t a = vbuf + hf * Sh::kBoxBytes + t * 128 + c * 16;
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+            for (int ks = 0; ks < KS; ++ks) {
+                qb[ks][0] = qrow[8 * ks + qd];
+                qb[ks][1] = qrow[8 * ks + 4 + qd];
             }
-            __syncwarp();
         }
 
-        // S^T = K Q^T : rows = tokens, cols = query heads of the group
-        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+        float oacc[KS][4];
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int t = lr + ((lj & 1) << 3);
-            const int chunk = 2 * ks + (lj >> 1);
-            const uint32_t a = kbuf + (chunk >> 3) * Sh::kBoxBytes + t * 128 +
-                               ((((chunk & 7) ^ (t & 7))) << 4);
-            uint32_t fr[4];
-            ldsm_x4(a, fr);
-            mma_bf16(sc, fr, qb[ks][0], qb[ks][1]);
-        }
-        // scores in base 2, masked past the end; sc[0..1] token g, sc[2..3] token g+8
-        const float x0 = g < nvalid ? sc[0] * p.scale_log2 : -INFINITY;
-        const float x1 = g < nvalid ? sc[1] * p.scale_log2 : -INFINITY;
-        const float x2 = g + 8 < nvalid ? sc[2] * p.scale_log2 : -INFINITY;
-        const float x3 = g + 8 < nvalid ? sc[3] * p.scale_log2 : -INFINITY;
-        float mx[2] = {fmaxf(x0, x2), fmaxf(x1, x3)};
+        for (int mt = 0; mt < KS; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
+        float m_run[2] = {-INFINITY, -INFINITY};
+        float l_acc[2] = {0.f, 0.f};
+
+        // ldmatrix row addresses: lane -> (matrix j = lane/8, row = lane%8)
+        const int lj = lane >> 3, lr = lane & 7;
+        const uint32_t head_off = warp * (kTok * 128);  // this head's 16 rows in a box
+
+        for (int i = 0; i < n_sub; ++i) {
+            const int st = i % NS;
+            if (!mbar_wait(bars + 8 * st, (i / NS) & 1)) {
+                raise_error(p.err, KF_DEVERR_TIMEOUT);
+                ok = false;
+                break;
+            }
+            const uint32_t kbuf = base + st * Sh::kStageBytes + head_off;
+            const uint32_t vbuf = kbuf + Sh::kHalves * Sh::kBoxBytes;
+            const int64_t t_base = (sb0 + i) * kTok;
+            const int64_t rem_tok = r.t_end - t_base;
+            const int nvalid = rem_tok < kTok ? (int)rem_tok : kTok;
+            bool wrote_smem = false;
+
+            if (FUSED && p_new >= t_base && p_new < t_base + kTok) {
+                // the step's append: this head's new K/V row into the stage and the cache
+                const int t = (int)(p_new - t_base);
+                constexpr int CH = D / 8;  // 16-byte chunks per row
+                if (lane < 2 * CH) {
+                    const bool is_v = lane >= CH;
+                    const int c = is_v ? lane - CH : lane;
+                    const uint4 val = reinterpret_cast<const uint4 *>(
+                        (is_v ? sp.v_new : sp.k_new) + ((int64_t)b * p.num_kv_heads + hkv) * D)[c];
+                    const uint32_t a = (is_v ? vbuf : kbuf) + (c >> 3) * Sh::kBoxBytes + t * 128 +
+                                       (((c & 7) ^ (t & 7)) << 4);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(val.x),
+                                 "r"(val.y), "r"(val.z), "r"(val.w)
+                                 : "memory");
+                    const int64_t phys = physical_block(p, b, p_new / p.block_size);
+                    const int64_t off = ((phys * p.block_size + p_new % p.block_size) * p.num_kv_heads + hkv) * D;
+                    reinterpret_cast<uint4 *>((is_v ? sp.v_cache : sp.k_cache) + off)[c] = val;
+                }
+                wrote_smem = true;
+                __syncwarp();
+            }
+            if (nvalid < kTok) {
+                // zero this head's V rows past the end (whole 128-byte rows, any swizzle)
+                for (int idx = lane; idx < (kTok - nvalid) * 8 * Sh::kHalves; idx += 32) {
+                    const int hf = idx / ((kTok - nvalid) * 8);
+                    const int rem = idx % ((kTok - nvalid) * 8);
+                    const int t = nvalid + rem / 8, c = rem % 8;
+                    const uint32_t a = vbuf + hf * Sh::kBoxBytes + t * 128 + c * 16;
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+                }
+                wrote_smem = true;
+                __syncwarp();
+            }
+
+            // S^T = K Q^T : rows = tokens, cols = query heads of the group
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
-            mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
-        }
+            for (int ks = 0; ks < KS; ++ks) {
+                const int t = lr + ((lj & 1) << 3);
+                const int chunk = 2 * ks + (lj >> 1);
+                const uint32_t a = kbuf + (chunk >> 3) * Sh::kBoxBytes + t * 128 +
+                                   ((((chunk & 7) ^ (t & 7))) << 4);
+                uint32_t fr[4];
+                ldsm_x4(a, fr);
+                mma_bf16(sc, fr, qb[ks][0], qb[ks][1]);
+            }
+            // scores in base 2, masked past the end; sc[0..1] token g, sc[2..3] token g+8
+            const float x0 = g < nvalid ? sc[0] * p.scale_log2 : -INFINITY;
+            const float x1 = g < nvalid ? sc[1] * p.scale_log2 : -INFINITY;
+            const float x2 = g + 8 < nvalid ? sc[2] * p.scale_log2 : -INFINITY;
+            const float x3 = g + 8 < nvalid ? sc[3] * p.scale_log2 : -INFINITY;
+            float mx[2] = {fmaxf(x0, x2), fmaxf(x1, x3)};
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            if (mx[j] > m_run[j] + kRescaleSlack) {
-                const float alpha = exp2f(m_run[j] - mx[j]);
-                m_run[j] = mx[j];
-                l_acc[j] *= alpha;
+            for (int off = 4; off < 32; off <<= 1) {
+                mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
+                mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
+            }
 #pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    oacc[mt][j] *= alpha;
-                    oacc[mt][j + 2] *= alpha;
+            for (int j = 0; j < 2; ++j) {
+                if (mx[j] > m_run[j] + kRescaleSlack) {
+                    const float alpha = exp2f(m_run[j] - mx[j]);
+                    m_run[j] = mx[j];
+                    l_acc[j] *= alpha;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        oacc[mt][j] *= alpha;
+                        oacc[mt][j + 2] *= alpha;
+                    }
                 }
             }
-        }
-        const float p0 = exp2f(x0 - m_run[0]), p1 = exp2f(x1 - m_run[1]);
-        const float p2 = exp2f(x2 - m_run[0]), p3 = exp2f(x3 - m_run[1]);
-        l_acc[0] += p0 + p2;
-        l_acc[1] += p1 + p3;
-        // P = P_hi + P_lo, both bf16: the PV product then carries ~16 bits of P
-        const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
-        const uint32_t r01 = pack_bf16(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-        const uint32_t r23 = pack_bf16(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
-        const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);  // P^T, tokens 0-7 / 8-15
-        const uint32_t bl0 = movmatrix_trans(r01), bl1 = movmatrix_trans(r23);
+            const float p0 = exp2f(x0 - m_run[0]), p1 = exp2f(x1 - m_run[1]);
+            const float p2 = exp2f(x2 - m_run[0]), p3 = exp2f(x3 - m_run[1]);
+            l_acc[0] += p0 + p2;
+            l_acc[1] += p1 + p3;
+            // P = P_hi + P_lo, both bf16: the PV product then carries ~16 bits of P
+            const uint32_t h01 = pack_bf16(p0, p1), h23 = pack_bf16(p2, p3);
+            const uint32_t r01 = pack_bf16(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+            const uint32_t r23 = pack_bf16(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+            const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);  // P^T, tokens 0-7 / 8-15
+            const uint32_t bl0 = movmatrix_trans(r01), bl1 = movmatrix_trans(r23);
 
-        // O^T += V^T P^T : rows = d, cols = query heads
+            // O^T += V^T P^T : rows = d, cols = query heads
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            const int t = lr + ((lj >> 1) << 3);
-            const int chunk = 2 * mt + (lj & 1);
-            const uint32_t a = vbuf + (chunk >> 3) * Sh::kBoxBytes + t * 128 +
-                               ((((chunk & 7) ^ (t & 7))) << 4);
-            uint32_t fr[4];
-            ldsm_x4_trans(a, fr);
-            mma_bf16(oacc[mt], fr, bh0, bh1);
-            mma_bf16(oacc[mt], fr, bl0, bl1);
+            for (int mt = 0; mt < KS; ++mt) {
+                const int t = lr + ((lj >> 1) << 3);
+                const int chunk = 2 * mt + (lj & 1);
+                const uint32_t a = vbuf + (chunk >> 3) * Sh::kBoxBytes + t * 128 +
+                                   ((((chunk & 7) ^ (t & 7))) << 4);
+                uint32_t fr[4];
+                ldsm_x4_trans(a, fr);
+                mma_bf16(oacc[mt], fr, bh0, bh1);
+                mma_bf16(oacc[mt], fr, bl0, bl1);
+            }
+            // generic smem writes above must be ordered before the next TMA into this stage
+            if (wrote_smem) fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + 8 * (NS + st));
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 8 * (NS + st));
-    }
-    if (!ok) return;
 
-    // finish: l over the 8 token lanes, then o = O / l and lse
+        if (ok) {
+            // finish: l over the 8 token lanes, then o = O / l and lse
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l_acc[0] += __shfl_xor_sync(0xffffffffu, l_acc[0], off);
-        l_acc[1] += __shfl_xor_sync(0xffffffffu, l_acc[1], off);
-    }
-    const int n0 = 2 * qd, n1 = 2 * qd + 1;
-    const float inv0 = 1.f / l_acc[0], inv1 = 1.f / l_acc[1];
-    float *o0 = p.out_partial + (row0 + (int64_t)warp * G + n0) * D;
-    float *o1 = o0 + D;
+            for (int off = 4; off < 32; off <<= 1) {
+                l_acc[0] += __shfl_xor_sync(0xffffffffu, l_acc[0], off);
+                l_acc[1] += __shfl_xor_sync(0xffffffffu, l_acc[1], off);
+            }
+            const int n0 = 2 * qd, n1 = 2 * qd + 1;
+            const float inv0 = 1.f / l_acc[0], inv1 = 1.f / l_acc[1];
+            const float lse0 = (m_run[0] + log2f(l_acc[0])) * 0.6931471805599453f;
+            const float lse1 = (m_run[1] + log2f(l_acc[1])) * 0.6931471805599453f;
+            // destination: the partial slot, or (fused, single split) the final rows
+            const bool direct = FUSED && n_ne == 1;
+            const int64_t prow = direct ? (int64_t)b * Hq + (int64_t)hq
+                                        : row0 + (int64_t)warp * G;  // row of query head n = 0
+            float *o_dst = FUSED ? (direct ? nullptr : sp.ws_o) : p.out_partial;
+            float *l_dst = FUSED ? (direct ? sp.lse_out : sp.ws_lse) : p.lse_partial;
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-        const int d0 = 16 * mt + g;
-        if (n0 < G) {
-            o0[d0] = oacc[mt][0] * inv0;
-            o0[d0 + 8] = oacc[mt][2] * inv0;
+            for (int mt = 0; mt < KS; ++mt) {
+                const int d0 = 16 * mt + g;
+                const float v00 = oacc[mt][0] * inv0, v01 = oacc[mt][2] * inv0;
+                const float v10 = oacc[mt][1] * inv1, v11 = oacc[mt][3] * inv1;
+                if (o_dst != nullptr) {
+                    if (n0 < G) {
+                        o_dst[(prow + n0) * D + d0] = v00;
+                        o_dst[(prow + n0) * D + d0 + 8] = v01;
+                    }
+                    if (n1 < G) {
+                        o_dst[(prow + n1) * D + d0] = v10;
+                        o_dst[(prow + n1) * D + d0 + 8] = v11;
+                    }
+                } else if (sp.out_dtype == KF_F32) {
+                    float *out = static_cast<float *>(sp.out);
+                    if (n0 < G) {
+                        out[(prow + n0) * D + d0] = v00;
+                        out[(prow + n0) * D + d0 + 8] = v01;
+                    }
+                    if (n1 < G) {
+                        out[(prow + n1) * D + d0] = v10;
+                        out[(prow + n1) * D + d0 + 8] = v11;
+                    }
+                } else {
+                    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(sp.out);
+                    if (n0 < G) {
+                        out[(prow + n0) * D + d0] = __float2bfloat16_rn(v00);
+                        out[(prow + n0) * D + d0 + 8] = __float2bfloat16_rn(v01);
+                    }
+                    if (n1 < G) {
+                        out[(prow + n1) * D + d0] = __float2bfloat16_rn(v10);
+                        out[(prow + n1) * D + d0 + 8] = __float2bfloat16_rn(v11);
+                    }
+                }
+            }
+            if (g == 0 && l_dst != nullptr) {
+                if (n0 < G) l_dst[prow + n0] = lse0;
+                if (n1 < G) l_dst[prow + n1] = lse1;
+            }
         }
-        if (n1 < G) {
-            o1[d0] = oacc[mt][1] * inv1;
-            o1[d0 + 8] = oacc[mt][3] * inv1;
-        }
+        if (!FUSED) return;
     }
-    if (g == 0) {
-        if (n0 < G) p.lse_partial[row0 + warp * G + n0] = (m_run[0] + log2f(l_acc[0])) * 0.6931471805599453f;
-        if (n1 < G) p.lse_partial[row0 + warp * G + n1] = (m_run[1] + log2f(l_acc[1])) * 0.6931471805599453f;
+
+    // ----------------------- fused: count, last CTA merges -----------------------
+    if (FUSED && n_ne > 1) {
+        __shared__ int sm_last;
+        __threadfence();  // this CTA's partial is visible before the count
+        __syncthreads();
+        unsigned int *ctr = sp.counters + (int64_t)b * p.num_kv_heads + hg;
+        if (threadIdx.x == 0) {
+            const unsigned int old = atomicAdd(ctr, 1u);
+            sm_last = old == (unsigned int)(n_ne - 1);
+            if (sm_last) *ctr = 0u;  // every other CTA of the group has counted: reset for the next step
+        }
+        __syncthreads();
+        if (sm_last) {
+            __threadfence();
+            if (ok) merge_group<D, HPC * G>(p, sp, b, h0 * G, n_ne, reinterpret_cast<float *>(smem_raw + (base - raw)));
+        }
     }
 }
 
@@ -380,9 +566,9 @@ bool encode_cache_map(EncodeFn fn, CUtensorMap *map, const void *cache, int64_t 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int HPC, int G, int NS>
-cudaError_t launch_t(const DecodeParams &p, cudaStream_t stream, const CUtensorMap &mk,
-                     const CUtensorMap &mv) {
+template <int D, int HPC, int G, int NS, bool FUSED>
+cudaError_t launch_t(const DecodeParams &p, const StepParams &sp, cudaStream_t stream,
+                     const CUtensorMap &mk, const CUtensorMap &mv) {
     using Sh = TcShape<D, HPC, NS>;
     // the dynamic shared-memory opt-in is per device; set it once per device
     static std::atomic<uint64_t> done{0};
@@ -391,13 +577,13 @@ cudaError_t launch_t(const DecodeParams &p, cudaStream_t stream, const CUtensorM
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(done.load() & bit)) {
-        e = cudaFuncSetAttribute(decode_tc_kernel<D, HPC, G, NS>,
+        e = cudaFuncSetAttribute(decode_tc_kernel<D, HPC, G, NS, FUSED>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmemBytes);
         if (e != cudaSuccess) return e;
         done.fetch_or(bit);
     }
     const dim3 grid(p.num_splits, p.num_kv_heads / HPC, p.batch);
-    decode_tc_kernel<D, HPC, G, NS><<<grid, Sh::kThreads, Sh::kSmemBytes, stream>>>(p, mk, mv);
+    decode_tc_kernel<D, HPC, G, NS, FUSED><<<grid, Sh::kThreads, Sh::kSmemBytes, stream>>>(p, sp, mk, mv);
     return cudaGetLastError();
 }
 
@@ -408,15 +594,15 @@ constexpr int stages_for() {
     return 2 * (D / 64) * 64 * kTok * HPC * 2 >= 32768 ? 3 : 4;
 }
 
-template <int D, int HPC>
-cudaError_t launch_g(const DecodeParams &p, cudaStream_t stream, const CUtensorMap &mk,
-                     const CUtensorMap &mv) {
+template <int D, int HPC, bool FUSED>
+cudaError_t launch_g(const DecodeParams &p, const StepParams &sp, cudaStream_t stream,
+                     const CUtensorMap &mk, const CUtensorMap &mv) {
     constexpr int NS = stages_for<D, HPC>();
     switch (p.num_q_heads / p.num_kv_heads) {
-        case 1: return launch_t<D, HPC, 1, NS>(p, stream, mk, mv);
-        case 2: return launch_t<D, HPC, 2, NS>(p, stream, mk, mv);
-        case 4: return launch_t<D, HPC, 4, NS>(p, stream, mk, mv);
-        case 8: return launch_t<D, HPC, 8, NS>(p, stream, mk, mv);
+        case 1: return launch_t<D, HPC, 1, NS, FUSED>(p, sp, stream, mk, mv);
+        case 2: return launch_t<D, HPC, 2, NS, FUSED>(p, sp, stream, mk, mv);
+        case 4: return launch_t<D, HPC, 4, NS, FUSED>(p, sp, stream, mk, mv);
+        case 8: return launch_t<D, HPC, 8, NS, FUSED>(p, sp, stream, mk, mv);
     }
     return cudaErrorInvalidValue;
 }
@@ -431,29 +617,31 @@ int heads_per_cta(int num_kv_heads) {
     return 1;
 }
 
+int tc_smem_bytes(int head_dim, int hpc) {
+    if (head_dim == 128) {
+        switch (hpc) {
+            case 8: return TcShape<128, 8, stages_for<128, 8>()>::kSmemBytes;
+            case 4: return TcShape<128, 4, stages_for<128, 4>()>::kSmemBytes;
+            case 2: return TcShape<128, 2, stages_for<128, 2>()>::kSmemBytes;
+            default: return TcShape<128, 1, stages_for<128, 1>()>::kSmemBytes;
+        }
+    }
+    switch (hpc) {
+        case 8: return TcShape<64, 8, stages_for<64, 8>()>::kSmemBytes;
+        case 4: return TcShape<64, 4, stages_for<64, 4>()>::kSmemBytes;
+        case 2: return TcShape<64, 2, stages_for<64, 2>()>::kSmemBytes;
+        default: return TcShape<64, 1, stages_for<64, 1>()>::kSmemBytes;
+    }
+}
+
 }  // namespace
 
 void decode_tc_shape(int num_kv_heads, int head_dim, int block_size, int *hpc_out,
                      int *ctas_per_sm) {
     (void)block_size;
     const int hpc = heads_per_cta(num_kv_heads);
-    int smem = 0;
-    if (head_dim == 128) {
-        switch (hpc) {
-            case 8: smem = TcShape<128, 8, stages_for<128, 8>()>::kSmemBytes; break;
-            case 4: smem = TcShape<128, 4, stages_for<128, 4>()>::kSmemBytes; break;
-            case 2: smem = TcShape<128, 2, stages_for<128, 2>()>::kSmemBytes; break;
-            default: smem = TcShape<128, 1, stages_for<128, 1>()>::kSmemBytes; break;
-        }
-    } else {
-        switch (hpc) {
-            case 8: smem = TcShape<64, 8, stages_for<64, 8>()>::kSmemBytes; break;
-            case 4: smem = TcShape<64, 4, stages_for<64, 4>()>::kSmemBytes; break;
-            case 2: smem = TcShape<64, 2, stages_for<64, 2>()>::kSmemBytes; break;
-            default: smem = TcShape<64, 1, stages_for<64, 1>()>::kSmemBytes; break;
-        }
-    }
-    const int per_sm = 228 * 1024;  // shared memory per SM, minus 1 KiB reserved per CTA below
+    const int smem = tc_smem_bytes(head_dim, hpc);
+    const int per_sm = 228 * 1024;  // shared memory per SM, 1 KiB of it reserved per CTA
     int c = per_sm / (smem + 1024);
     if (c > 8) c = 8;
     if (c < 1) c = 1;
@@ -461,7 +649,14 @@ void decode_tc_shape(int num_kv_heads, int head_dim, int block_size, int *hpc_ou
     *ctas_per_sm = c;
 }
 
-cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream, void *encode) {
+int decode_tc_ring_bytes(int num_kv_heads, int head_dim) {
+    const int hpc = heads_per_cta(num_kv_heads);
+    return tc_smem_bytes(head_dim, hpc) - 1024 - 16 * 4;  // minus alignment slack and barriers
+}
+
+template <bool FUSED>
+static cudaError_t launch_any(const DecodeParams &p, const StepParams &sp, cudaStream_t stream,
+                              void *encode) {
     if (p.batch == 0) return cudaSuccess;
     const int hpc = heads_per_cta(p.num_kv_heads);
     EncodeFn fn = reinterpret_cast<EncodeFn>(encode);
@@ -473,18 +668,39 @@ cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream, void *e
         return cudaErrorInvalidValue;
     if (p.head_dim == 128) {
         switch (hpc) {
-            case 8: return launch_g<128, 8>(p, stream, mk, mv);
-            case 4: return launch_g<128, 4>(p, stream, mk, mv);
-            case 2: return launch_g<128, 2>(p, stream, mk, mv);
-            default: return launch_g<128, 1>(p, stream, mk, mv);
+            case 8: return launch_g<128, 8, FUSED>(p, sp, stream, mk, mv);
+            case 4: return launch_g<128, 4, FUSED>(p, sp, stream, mk, mv);
+            case 2: return launch_g<128, 2, FUSED>(p, sp, stream, mk, mv);
+            default: return launch_g<128, 1, FUSED>(p, sp, stream, mk, mv);
         }
     }
     switch (hpc) {
-        case 8: return launch_g<64, 8>(p, stream, mk, mv);
-        case 4: return launch_g<64, 4>(p, stream, mk, mv);
-        case 2: return launch_g<64, 2>(p, stream, mk, mv);
-        default: return launch_g<64, 1>(p, stream, mk, mv);
+        case 8: return launch_g<64, 8, FUSED>(p, sp, stream, mk, mv);
+        case 4: return launch_g<64, 4, FUSED>(p, sp, stream, mk, mv);
+        case 2: return launch_g<64, 2, FUSED>(p, sp, stream, mk, mv);
+        default: return launch_g<64, 1, FUSED>(p, sp, stream, mk, mv);
     }
+}
+
+cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream, void *encode) {
+    StepParams sp = {};
+    return launch_any<false>(p, sp, stream, encode);
+}
+
+cudaError_t launch_decode_step_tc(const DecodeParams &p, const StepArgs &a, cudaStream_t stream,
+                                  void *encode) {
+    StepParams sp;
+    sp.k_new = a.k_new;
+    sp.v_new = a.v_new;
+    sp.k_cache = a.k_cache;
+    sp.v_cache = a.v_cache;
+    sp.ws_o = a.ws_o;
+    sp.ws_lse = a.ws_lse;
+    sp.counters = a.counters;
+    sp.out = a.out;
+    sp.lse_out = a.lse_out;
+    sp.out_dtype = a.out_dtype;
+    return launch_any<true>(p, sp, stream, encode);
 }
 
 }  // namespace kf

@@ -32,9 +32,27 @@ struct DecodeParams {
     float scale_log2;         // scale * log2(e)
 };
 
+// Extra arguments of the single-launch decode step (append + attention + merge).
+struct StepArgs {
+    const uint16_t *k_new;   // bf16 [B, Hkv, D]
+    const uint16_t *v_new;
+    uint16_t *k_cache;       // written at each request's new position
+    uint16_t *v_cache;
+    float *ws_o;             // workspace partials [S, B, Hq, D]
+    float *ws_lse;           // workspace lse [S, B, Hq]
+    unsigned int *counters;  // workspace [B, Hkv], zero between steps
+    void *out;               // [B, Hq, D] of out_dtype
+    float *lse_out;          // [B, Hq] or null
+    int out_dtype;
+};
+
 // Decode kernels, one per implementation. Each returns the launch status.
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream, void *encode_fn);
+cudaError_t launch_decode_step_tc(const DecodeParams &p, const StepArgs &a, cudaStream_t stream,
+                                  void *encode_fn);
+// Bytes of the tensor-core kernel's shared-memory ring (the fused merge reuses it).
+int decode_tc_ring_bytes(int num_kv_heads, int head_dim);
 // Largest number of resident CTAs per SM and KV heads per CTA the tensor-core
 // kernel uses for this shape (for the split planner).
 void decode_tc_shape(int num_kv_heads, int head_dim, int block_size, int *heads_per_cta,

@@ -10,9 +10,11 @@
 // KernelFlume (academ.us/article/2606.29207) section 5.1: merging the
 // partials of a partition of the tokens equals attention over all of them.
 //
-// Mapping: D/4 threads per (b, h) row, each owning 4 consecutive outputs, so
-// every partial row is read as coalesced 16-byte vectors; the lse column is
-// read once per thread (the reads of one row hit the same line).
+// Mapping: one CTA per (b, h) row; P groups of D/4 threads each take every
+// P-th partial (so S partials are read P at a time, coalesced 16-byte vectors,
+// 4 loads in flight per thread), then the groups' sums are combined in shared
+// memory. The row max M is found first by all threads striding over the S
+// lse values.
 #include <math.h>
 
 #include "kf_internal.cuh"
@@ -20,22 +22,36 @@
 namespace kf {
 namespace {
 
+constexpr int kGroups = 8;  // partial groups per row
+
 template <int D>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kGroups *(D / 4))
 merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part, int S,
              int64_t rows, void *__restrict__ out, int out_dtype, float *__restrict__ lse_out) {
-    constexpr int TPR = D / 4;  // threads per row
-    const int64_t row = (int64_t)blockIdx.x * (blockDim.x / TPR) + threadIdx.x / TPR;
-    const int c = threadIdx.x % TPR;
-    if (row >= rows) return;
+    constexpr int TPR = D / 4;  // threads per group: 4 outputs each
+    const int64_t row = blockIdx.x;
+    const int c = threadIdx.x % TPR, grp = threadIdx.x / TPR;
 
+    __shared__ float sm_red[kGroups * TPR / 32 + 1];
+    __shared__ __align__(16) float4 sm_acc[kGroups][TPR];
+    __shared__ float sm_w[kGroups];
+
+    // 1. M = max_s lse_s
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, lse_part[(int64_t)s * rows + row]);
+    for (int s = threadIdx.x; s < S; s += blockDim.x) M = fmaxf(M, lse_part[(int64_t)s * rows + row]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if ((threadIdx.x & 31) == 0) sm_red[threadIdx.x >> 5] = M;
+    __syncthreads();
+    M = -INFINITY;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) M = fmaxf(M, sm_red[i]);
 
+    // 2. this group's share of sum_s w_s o_s and sum_s w_s
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < S; ++s) {
+#pragma unroll 4
+        for (int s = grp; s < S; s += kGroups) {
             const float l = lse_part[(int64_t)s * rows + row];
             if (l == -INFINITY) continue;  // empty partial: weight 0, o not read
             const float w = expf(l - M);
@@ -46,6 +62,22 @@ merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_par
             acc.w = fmaf(w, o.w, acc.w);
             wsum += w;
         }
+    }
+    sm_acc[grp][c] = acc;
+    if (c == 0) sm_w[grp] = wsum;
+    __syncthreads();
+    if (grp != 0) return;
+
+    // 3. combine the groups and write
+    wsum = 0.f;
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+        const float4 a = sm_acc[g][c];
+        acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
+        wsum += sm_w[g];
+    }
+    if (M != -INFINITY) {
         const float inv = 1.f / wsum;
         acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
     }
@@ -69,16 +101,13 @@ cudaError_t launch_merge(const float *out_partial, const float *lse_partial, int
                          float *lse_out, cudaStream_t stream) {
     const int64_t rows = (int64_t)batch * num_q_heads;
     if (rows == 0) return cudaSuccess;
-    const int threads = 128;
-    if (head_dim == 128) {
-        const int64_t rpb = threads / 32;
-        merge_kernel<128><<<(unsigned)((rows + rpb - 1) / rpb), threads, 0, stream>>>(
+    if (rows > 0x7fffffff) return cudaErrorInvalidValue;
+    if (head_dim == 128)
+        merge_kernel<128><<<(unsigned)rows, kGroups * 32, 0, stream>>>(
             out_partial, lse_partial, num_partials, rows, out, out_dtype, lse_out);
-    } else {
-        const int64_t rpb = threads / 16;
-        merge_kernel<64><<<(unsigned)((rows + rpb - 1) / rpb), threads, 0, stream>>>(
+    else
+        merge_kernel<64><<<(unsigned)rows, kGroups * 16, 0, stream>>>(
             out_partial, lse_partial, num_partials, rows, out, out_dtype, lse_out);
-    }
     return cudaGetLastError();
 }
 

@@ -44,6 +44,11 @@ _lib.kf_choose_num_splits_for.restype = _i32
 _lib.kf_choose_num_splits_for.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _i32]
 _lib.kf_merge_partials.restype = _i32
 _lib.kf_merge_partials.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
+_lib.kf_decode_step_workspace_size.restype = ctypes.c_size_t
+_lib.kf_decode_step_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
+_lib.kf_decode_step.restype = _i32
+_lib.kf_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                _i32, _i64, _f32, _i32, _vp, ctypes.c_size_t, _vp, _i32, _vp, _vp]
 _lib.kf_get_device_error.restype = _i32
 _lib.kf_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), _vp]
 _lib.kf_status_string.restype = ctypes.c_char_p
@@ -166,6 +171,49 @@ def kf_merge_partials(out_partial: torch.Tensor, lse_partial: torch.Tensor,
         S, B, hq, d, _dev(out, out.dtype, "out"), code,
         None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
         "kf_merge_partials")
+    return out, lse_out
+
+
+def kf_decode_step_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                                  num_splits: int) -> int:
+    return int(_lib.kf_decode_step_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, num_splits))
+
+
+def make_workspace(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, num_splits: int,
+                   device=None) -> torch.Tensor:
+    """A zero-filled workspace for kf_decode_step (the zero fill is required once)."""
+    n = kf_decode_step_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, num_splits)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def kf_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                   v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens_before: torch.Tensor,
+                   max_context_len: int, scale: float, num_splits: int,
+                   workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                   out_dtype=torch.float32, lse_out: Optional[torch.Tensor] = None, want_lse: bool = True,
+                   stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Append + split attention + merge in one launch; returns (out, lse)."""
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
+    code = {torch.float32: KF_F32, torch.bfloat16: KF_BF16}.get(out.dtype)
+    if code is None:
+        raise ValueError("out must be float32 or bfloat16")
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+    if workspace is None and num_splits > 1:
+        raise ValueError("num_splits > 1 needs a workspace (make_workspace)")
+    ws_ptr = None if workspace is None else _dev(workspace, torch.uint8, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel()
+    _check(_lib.kf_decode_step(
+        _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
+        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _dev(context_lens_before, torch.int32, "context_lens_before"), int(max_context_len), B, hq, hkv, d,
+        bs, nb, float(scale), int(num_splits), ws_ptr, ws_bytes, _dev(out, out.dtype, "out"), code,
+        None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
+        "kf_decode_step")
     return out, lse_out
 
 

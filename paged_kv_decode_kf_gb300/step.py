@@ -19,12 +19,19 @@ from .workloads import DecodeInputs
 
 
 class DecodeStep:
+    """One decode step over `inp`. fused=True runs kf_decode_step (one launch;
+    not for sharded workloads); otherwise kf_append_kv, one
+    kf_paged_decode_attention per token-range view, kf_merge_partials."""
+
     def __init__(self, inp: DecodeInputs, num_splits: Optional[int] = None,
-                 out_dtype=torch.float32, with_append: bool = True):
+                 out_dtype=torch.float32, with_append: bool = True, fused: bool = False):
         self.inp = inp
         w = inp.workload
         self.w = w
         self.with_append = with_append
+        if fused and (w.shards or not with_append):
+            raise ValueError("the single-launch step covers unsharded workloads with the append")
+        self.fused = fused
         B, Hq, D = w.batch, w.num_q_heads, w.head_dim
         dev = inp.q.device
         if w.shards:
@@ -39,6 +46,9 @@ class DecodeStep:
         self.lse_partial = torch.empty((slots, B, Hq), dtype=torch.float32, device=dev)
         self.out = torch.empty((B, Hq, D), dtype=out_dtype, device=dev)
         self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        self.workspace = None
+        if fused:
+            self.workspace = kf.make_workspace(B, Hq, w.num_kv_heads, D, self.num_splits, dev)
 
     def plan(self, ctx_lens: torch.Tensor, max_ctx: int) -> int:
         w = self.w
@@ -62,7 +72,16 @@ class DecodeStep:
     def merge(self, stream=None) -> None:
         kf.kf_merge_partials(self.out_partial, self.lse_partial, self.out, lse_out=self.lse, stream=stream)
 
+    def step_fused(self, stream=None) -> None:
+        i = self.inp
+        kf.kf_decode_step(i.q, i.k_new, i.v_new, i.k_cache, i.v_cache, i.block_tables, i.ctx_before,
+                          i.max_ctx_after, self.w.scale, self.num_splits, self.workspace, self.out,
+                          lse_out=self.lse, stream=stream)
+
     def run(self, stream=None) -> None:
+        if self.fused:
+            self.step_fused(stream)
+            return
         if self.with_append:
             self.append(stream)
         self.attention(stream)
@@ -70,4 +89,6 @@ class DecodeStep:
 
     @property
     def launches_per_step(self) -> int:
+        if self.fused:
+            return 1
         return int(self.with_append) + len(self.views) + 1

@@ -132,3 +132,28 @@ def test_binding_rejects_host_tensors(kf):
         kf.kf_paged_decode_attention(q, q, q, torch.zeros(2, 4, dtype=torch.int32),
                                      torch.ones(2, dtype=torch.int32), 4, 0.1, 1,
                                      out_partial=torch.zeros(1), lse_partial=torch.zeros(1))
+
+
+def test_decode_step_host_checks(kf):
+    lib = kf.raw()
+    need = kf.kf_decode_step_workspace_size(4, 32, 8, 128, 10)
+    al = lambda x: (x + 255) // 256 * 256
+    assert need == al(10 * 4 * 32 * 128 * 4) + al(10 * 4 * 32 * 4) + al(4 * 8 * 4)
+    assert kf.kf_decode_step_workspace_size(0, 32, 8, 128, 1) == al(0) + al(0) + al(0)
+    assert kf.kf_decode_step_workspace_size(4, 32, 8, 128, 0) == 0
+
+    def step(**kw):
+        a = dict(q=16, kn=16, vn=16, kc=16, vc=16, bt=16, st=8, ctx=16, mc=100, B=4, hq=32, hkv=8, d=128, bs=16,
+                 nb=64, scale=0.1, S=10, ws=16, wsb=need, out=16, dt=kf.KF_F32, lse=None)
+        a.update(kw)
+        return lib.kf_decode_step(a["q"], a["kn"], a["vn"], a["kc"], a["vc"], a["bt"], a["st"], a["ctx"], a["mc"],
+                                  a["B"], a["hq"], a["hkv"], a["d"], a["bs"], a["nb"], a["scale"], a["S"], a["ws"],
+                                  a["wsb"], a["out"], a["dt"], a["lse"], None)
+    assert step(B=0) == kf.KF_OK
+    for bad in (dict(ws=None), dict(wsb=need - 1), dict(ws=8), dict(kn=None), dict(out=None), dict(dt=3),
+                dict(S=0), dict(mc=-1), dict(scale=float("nan"))):
+        assert step(**bad) == kf.KF_ERR_INVALID, bad
+    assert step(S=100000) == kf.KF_ERR_UNSUPPORTED
+    big = kf.kf_decode_step_workspace_size(4, 32, 8, 128, 2000)
+    assert step(S=2000, wsb=big) == kf.KF_ERR_UNSUPPORTED     # the merge would not fit in shared memory
+    assert step(d=96) == kf.KF_ERR_UNSUPPORTED
