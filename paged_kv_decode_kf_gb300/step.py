@@ -34,10 +34,12 @@ class DecodeStep:
         self.fused = fused
         B, Hq, D = w.batch, w.num_q_heads, w.head_dim
         dev = inp.q.device
+        # host-side bounds, computed once: reading them per step would synchronise
+        self.max_ctx = inp.max_ctx_after
         if w.shards:
             self.views = [(s.block_tables, s.ctx_after, int(s.ctx_after.max().item())) for s in inp.shards]
         else:
-            self.views = [(inp.block_tables, inp.ctx_after, inp.max_ctx_after)]
+            self.views = [(inp.block_tables, inp.ctx_after, self.max_ctx)]
         if num_splits is None:
             num_splits = max(self.plan(v[1], v[2]) for v in self.views)
         self.num_splits = int(num_splits)
@@ -75,7 +77,7 @@ class DecodeStep:
     def step_fused(self, stream=None) -> None:
         i = self.inp
         kf.kf_decode_step(i.q, i.k_new, i.v_new, i.k_cache, i.v_cache, i.block_tables, i.ctx_before,
-                          i.max_ctx_after, self.w.scale, self.num_splits, self.workspace, self.out,
+                          self.max_ctx, self.w.scale, self.num_splits, self.workspace, self.out,
                           lse_out=self.lse, stream=stream)
 
     def run(self, stream=None) -> None:
