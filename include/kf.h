@@ -237,6 +237,41 @@ kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, vo
                          kf_stream_t stream);
 
 /*
+ * kf_decode_step_static -- kf_decode_step without a caller-provided workspace,
+ * for callers that may not allocate device memory.
+ *
+ * The paged-decode pages have no counterpart to this call; it exists for
+ * users of this library whose device memory is reserved up front by their
+ * own pool allocator, plugin hosts that pass a library only the buffers of
+ * each call, and decode loops that cannot afford cudaMalloc's implicit device
+ * synchronisation. It computes exactly what kf_decode_step computes (same
+ * arguments, minus the workspace), and allocates nothing: its scratch is a
+ * KF_STATIC_SCRATCH_BYTES array in the library's own device memory, which
+ * every GPU that loads the library keeps until the process exits.
+ *
+ * Limits and behaviour:
+ *  - Calls whose kf_decode_step_workspace_size(...) exceeds
+ *    KF_STATIC_SCRATCH_BYTES return KF_ERR_UNSUPPORTED (use kf_decode_step with
+ *    your own workspace, or fewer splits).
+ *  - The first call on a device looks up the array's device address (a
+ *    one-time set-up on that device); make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one array, which keeps the previous
+ *    call's contents; each call clears the part that must start at zero (the
+ *    merge counters) on its own stream. Calls that overlap on the GPU (on
+ *    different streams, or from different threads) race on the array and
+ *    give wrong results: serialise them.
+ */
+#define KF_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+kf_status kf_decode_step_static(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                                void *v_cache, const int32_t *block_tables, int bt_stride,
+                                const int32_t *context_lens_before, int max_context_len, int batch,
+                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int64_t num_blocks, float scale, int num_splits, void *out,
+                                kf_dtype out_dtype, float *lse_out, kf_stream_t stream);
+
+/*
  * kf_get_device_error -- read and clear the current device's error word.
  *
  * Synchronises `stream`, copies the word (KF_DEVERR_* bits) to *flags and

@@ -49,6 +49,10 @@ _lib.kf_decode_step_workspace_size.argtypes = [_i32, _i32, _i32, _i32, _i32]
 _lib.kf_decode_step.restype = _i32
 _lib.kf_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                 _i32, _i64, _f32, _i32, _vp, ctypes.c_size_t, _vp, _i32, _vp, _vp]
+_lib.kf_decode_step_static.restype = _i32
+_lib.kf_decode_step_static.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                       _i32, _i32, _i64, _f32, _i32, _vp, _i32, _vp, _vp]
+KF_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
 _lib.kf_get_device_error.restype = _i32
 _lib.kf_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), _vp]
 _lib.kf_status_string.restype = ctypes.c_char_p
@@ -215,6 +219,29 @@ def kf_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_
         None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
         "kf_decode_step")
     return out, lse_out
+
+
+def kf_decode_step_static(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                          k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                          context_lens_before: torch.Tensor, max_context_len: int, scale: float,
+                          num_splits: int, out: torch.Tensor, lse_out: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
+    """kf_decode_step with the library's own fixed scratch instead of a workspace,
+    for callers that may not allocate device memory; `out` (and `lse_out`) must
+    be given. Calls on one device must not overlap on the GPU."""
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    code = {torch.float32: KF_F32, torch.bfloat16: KF_BF16}.get(out.dtype)
+    if code is None:
+        raise ValueError("out must be float32 or bfloat16")
+    _check(_lib.kf_decode_step_static(
+        _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
+        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _dev(context_lens_before, torch.int32, "context_lens_before"), int(max_context_len), B, hq, hkv, d,
+        bs, nb, float(scale), int(num_splits), _dev(out, out.dtype, "out"), code,
+        None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
+        "kf_decode_step_static")
 
 
 def kf_get_device_error(stream=None) -> int:
