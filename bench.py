@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--path", default="auto", choices=["auto", "fused", "calls"],
                     help="fused: kf_decode_step (one launch); calls: append, attention, merge; "
                          "auto: fused for unsharded workloads with the tensor-core kernel")
+    ap.add_argument("--num-splits", type=int, default=None,
+                    help="override the planner's split count (tuning sweeps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -302,7 +304,7 @@ def run_ours(args):
     W = max(args.warmup, 3)
     dev = wl.make_inputs(w, "cuda:%d" % local)
     fused = args.path == "fused" or (args.path == "auto" and not w.shards and args.decode_kernel == "tc")
-    step = DecodeStep(dev, fused=fused)
+    step = DecodeStep(dev, num_splits=args.num_splits, fused=fused)
     kv_bytes = dev.kv_bytes()
     stream = torch.cuda.current_stream()
 
@@ -428,6 +430,8 @@ def run_ours(args):
                        "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
                        "block_size": w.block_size, "num_splits": step.num_splits,
                        "kv_bytes_per_step": kv_bytes, "decode_kernel": args.decode_kernel,
+                       "heads_per_cta_override": os.environ.get("KF_TC_HPC"),
+                       "num_splits_source": "planner" if args.num_splits is None else "--num-splits",
                        "step": "append + split attention + LSE merge",
                        "path": "kf_decode_step (one launch)" if step.fused else
                                "kf_append_kv + kf_paged_decode_attention x%d + kf_merge_partials" % n_att,

@@ -206,31 +206,64 @@ __device__ void merge_group(const DecodeParams &p, const StepParams &sp, int b, 
         sm_sum[r] = sum;
     }
     __syncthreads();
+    // each thread owns up to U (row, 4-column) units and walks the partials in
+    // batches of SB, keeping U*SB 16-byte loads in flight before it sums them
     constexpr int C = D / 4;
-    for (int u = tid; u < R * C; u += nt) {
-        const int r = u / C, c = u % C;
-        const int64_t row = (int64_t)b * p.num_q_heads + row_first + r;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int s = 0; s < n_ne; ++s) {
-            const float w = sm_w[s * R + r];
-            const float4 o = __ldcg(reinterpret_cast<const float4 *>(sp.ws_o + ((int64_t)s * rows + row) * D) + c);
-            acc.x = fmaf(w, o.x, acc.x);
-            acc.y = fmaf(w, o.y, acc.y);
-            acc.z = fmaf(w, o.z, acc.z);
-            acc.w = fmaf(w, o.w, acc.w);
+    constexpr int U = 4, SB = 4;
+    for (int u0 = tid; u0 < R * C; u0 += nt * U) {
+        float4 acc[U];
+        int64_t rowu[U];
+        bool live[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int u = u0 + k * nt;
+            live[k] = u < R * C;
+            rowu[k] = (int64_t)b * p.num_q_heads + row_first + (live[k] ? u / C : 0);
+            acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const float inv = 1.f / sm_sum[r];
-        acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-        if (sp.out_dtype == KF_F32) {
-            reinterpret_cast<float4 *>(static_cast<float *>(sp.out) + row * D)[c] = acc;
-        } else {
-            uint2 v;
-            v.x = pack_bf16(acc.x, acc.y);
-            v.y = pack_bf16(acc.z, acc.w);
-            reinterpret_cast<uint2 *>(static_cast<uint16_t *>(sp.out) + row * D)[c] = v;
+        for (int s0 = 0; s0 < n_ne; s0 += SB) {
+            float4 o[SB][U];
+#pragma unroll
+            for (int j = 0; j < SB; ++j)
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const int u = u0 + k * nt;
+                    o[j][k] = (live[k] && s0 + j < n_ne)
+                                  ? __ldcg(reinterpret_cast<const float4 *>(
+                                               sp.ws_o + ((int64_t)(s0 + j) * rows + rowu[k]) * D) + u % C)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int j = 0; j < SB; ++j)
+#pragma unroll
+                for (int k = 0; k < U; ++k) {
+                    const int u = u0 + k * nt;
+                    const float w = (live[k] && s0 + j < n_ne) ? sm_w[(s0 + j) * R + u / C] : 0.f;
+                    acc[k].x = fmaf(w, o[j][k].x, acc[k].x);
+                    acc[k].y = fmaf(w, o[j][k].y, acc[k].y);
+                    acc[k].z = fmaf(w, o[j][k].z, acc[k].z);
+                    acc[k].w = fmaf(w, o[j][k].w, acc[k].w);
+                }
         }
-        if (c == 0 && sp.lse_out) sp.lse_out[row] = sm_m[r] + logf(sm_sum[r]);
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            if (!live[k]) continue;
+            const int u = u0 + k * nt;
+            const int r = u / C, c = u % C;
+            const int64_t row = rowu[k];
+            const float inv = 1.f / sm_sum[r];
+            float4 a = acc[k];
+            a.x *= inv; a.y *= inv; a.z *= inv; a.w *= inv;
+            if (sp.out_dtype == KF_F32) {
+                reinterpret_cast<float4 *>(static_cast<float *>(sp.out) + row * D)[c] = a;
+            } else {
+                uint2 v;
+                v.x = pack_bf16(a.x, a.y);
+                v.y = pack_bf16(a.z, a.w);
+                reinterpret_cast<uint2 *>(static_cast<uint16_t *>(sp.out) + row * D)[c] = v;
+            }
+            if (c == 0 && sp.lse_out) sp.lse_out[row] = sm_m[r] + logf(sm_sum[r]);
+        }
     }
 }
 
