@@ -65,6 +65,20 @@ def _declare(lib) -> None:
     lib.kfo_merge_partials.restype = None
     lib.kfo_merge_partials.argtypes = [_f64p, _f64p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, _f64p, _f64p]
+    _u8p = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
+    _f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+    lib.kfo_e4m3_to_double.restype = ctypes.c_double
+    lib.kfo_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.kfo_e4m3_from_float.restype = ctypes.c_uint8
+    lib.kfo_e4m3_from_float.argtypes = [ctypes.c_float]
+    lib.kfo_decode_partials_fp8.restype = ctypes.c_int
+    lib.kfo_decode_partials_fp8.argtypes = [
+        _u16p, _u8p, _u8p, _f32p, _f32p, _i32p, ctypes.c_int, _i32p, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_int,
+        ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, _f64p, _f64p]
+    lib.kfo_append_fp8.restype = ctypes.c_int
+    lib.kfo_append_fp8.argtypes = [_u8p, _u8p, _u16p, _u16p, _f32p, _f32p, _i32p, ctypes.c_int, _i32p,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64]
     lib.kfo_append.restype = ctypes.c_int
     lib.kfo_append.argtypes = [_u16p, _u16p, _u16p, _u16p, _i32p, ctypes.c_int, _i32p, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64]
@@ -211,3 +225,67 @@ def append(k_cache, v_cache, k_new, v_new, block_tables, ctx_before,
     skipped = (lib or load()).kfo_append(k2, v2, _u16(k_new), _u16(v_new), bt, bt.shape[1], ctx,
                                          bt.shape[0], hkv, d, bs, nb)
     return k2, v2, skipped
+
+
+# ----------------------------------------------------------------------------
+# FP8 (E4M3) KV cache
+# ----------------------------------------------------------------------------
+
+def e4m3_to_f64(code: int, lib=None) -> float:
+    return (lib or load()).kfo_e4m3_to_double(int(code))
+
+
+def e4m3_from_f32(x: float, lib=None) -> int:
+    return int((lib or load()).kfo_e4m3_from_float(float(x)))
+
+
+def _u8(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == np.uint8, a.dtype
+    return a
+
+
+def decode_partials_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, ctx_lens, scale: float,
+                        num_splits: int, max_context_len: Optional[int] = None,
+                        rows: Optional[Sequence] = None, lib=None) -> Tuple[np.ndarray, np.ndarray]:
+    """Partials over an E4M3 cache (uint8 codes) with per-KV-head fp32 scales."""
+    q, k_cache, v_cache = _u16(q), _u8(k_cache), _u8(v_cache)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    bt, ctx = _i32(block_tables), _i32(ctx_lens)
+    B, Hq, D = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if max_context_len is None:
+        max_context_len = int(ctx.max()) if B else 0
+    o = np.full((num_splits, B, Hq, D), np.nan, dtype=np.float64)
+    lse = np.full((num_splits, B, Hq), np.nan, dtype=np.float64)
+    rows_arr, n_rows = None, 0
+    if rows is not None:
+        rows_arr = _i32(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+        n_rows = rows_arr.shape[0]
+    rc = (lib or load()).kfo_decode_partials_fp8(
+        q, k_cache, v_cache, ks, vs, bt, bt.shape[1], ctx, B, Hq, hkv, D, bs, nb, scale, num_splits,
+        max_context_len, None if rows_arr is None else rows_arr.ctypes.data, n_rows, o, lse)
+    if rc != 0:
+        raise ValueError("oracle decode_partials_fp8 failed (rc=%d)" % rc)
+    return o, lse
+
+
+def attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, ctx_lens, scale: float,
+                  rows: Optional[Sequence] = None, lib=None) -> Tuple[np.ndarray, np.ndarray]:
+    o, lse = decode_partials_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, ctx_lens, scale, 1,
+                                 rows=rows, lib=lib)
+    return o[0], lse[0]
+
+
+def append_fp8(k_cache, v_cache, k_new, v_new, k_scale, v_scale, block_tables, ctx_before,
+               lib=None) -> Tuple[np.ndarray, np.ndarray, int]:
+    """Copies of E4M3 caches with each request's new rows quantised in."""
+    k2, v2 = _u8(k_cache).copy(), _u8(v_cache).copy()
+    nb, bs, hkv, d = k2.shape
+    bt, ctx = _i32(block_tables), _i32(ctx_before)
+    skipped = (lib or load()).kfo_append_fp8(
+        k2, v2, _u16(k_new), _u16(v_new), np.ascontiguousarray(k_scale, dtype=np.float32),
+        np.ascontiguousarray(v_scale, dtype=np.float32), bt, bt.shape[1], ctx, bt.shape[0], hkv, d, bs, nb)
+    return k2, v2, skipped
+

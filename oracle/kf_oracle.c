@@ -36,6 +36,16 @@
  *    next position before attending (KernelFlume section 3.2, "Local
  *    attention on the attention nodes").
  *
+ *  - FP8 KV cache: the decode posts on blog.lo0.es ("Quantised KV cache --
+ *    --kv-cache-dtype fp8") store K/V in 8-bit floats with scales to halve the
+ *    bytes decode reads. Here a cached element is an OCP FP8 E4M3 code c with
+ *    a per-KV-head fp32 scale; its value is decode(c) * scale. The append
+ *    quantises: c = E4M3 round-to-nearest-even, saturating to +-448, of the
+ *    fp32 quotient float(x) / scale. E4M3 (OCP 8-bit floating point
+ *    specification): 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent
+ *    field 0 is subnormal (m * 2^-9); S.1111.111 is NaN; no infinities; the
+ *    largest finite magnitude is 1.75 * 2^8 = 448.
+ *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - query head h reads KV head h / G with G = num_q_heads / num_kv_heads
  *    (contiguous groups);
@@ -339,3 +349,195 @@ int kfo_append(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new, cons
     }
     return skipped;
 }
+
+/* ------------------------------------------------------------------------- */
+/* FP8 (E4M3) KV cache                                                        */
+/* ------------------------------------------------------------------------- */
+
+/* Value of an E4M3 code (NaN for S.1111.111). */
+double kfo_e4m3_to_double(uint8_t code)
+{
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);              /* subnormal: m/8 * 2^-6 */
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* E4M3 code of x: round to nearest, ties to even, saturating to +-448; NaN -> 0x7F. */
+uint8_t kfo_e4m3_from_float(float xf)
+{
+    double x = (double)xf;
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    /* quantum of the binade holding a: 2^-9 below 2^-6, else 2^(e-3) */
+    int e = a > 0 ? (int)floor(log2(a)) : -7;
+    if (e < -6)
+        e = -6;
+    double quantum = ldexp(1.0, e - 3);
+    double q = a / quantum;                  /* exact: a power-of-two scaling */
+    double fl = floor(q);
+    double frac = q - fl;
+    double n = fl;
+    if (frac > 0.5 || (frac == 0.5 && fmod(fl, 2.0) == 1.0))
+        n = fl + 1.0;
+    /* n in [0, 16]: back to exponent/mantissa fields */
+    double v = n * quantum;
+    if (v >= 448.0)
+        return sign | 0x7E;
+    if (v == 0.0)
+        return sign;
+    int ev = (int)floor(log2(v));
+    if (ev < -6) {                           /* subnormal: v = m * 2^-9 */
+        return sign | (uint8_t)(v / ldexp(1.0, -9));
+    }
+    int mant = (int)(v / ldexp(1.0, ev - 3)) - 8;
+    return sign | (uint8_t)(((ev + 7) << 3) | mant);
+}
+
+/* Offset helper for a byte cache [num_blocks, block_size, num_kv_heads, head_dim]. */
+static int64_t cache_row8(int64_t block, int64_t slot, int kv_head,
+                          int block_size, int num_kv_heads, int head_dim)
+{
+    return ((block * block_size + slot) * num_kv_heads + kv_head) * (int64_t)head_dim;
+}
+
+/*
+ * Attention of one query row over tokens [t_begin, t_end) of an FP8 cache:
+ * the same definition as kfo_partial with K_t = decode(k code) * k_scale and
+ * V_t = decode(v code) * v_scale (the scales of this KV head).
+ */
+int kfo_partial_fp8(const uint16_t *q_row, const uint8_t *k_cache, const uint8_t *v_cache,
+                    double k_scale, double v_scale, const int32_t *bt_row, int64_t num_blocks,
+                    int block_size, int num_kv_heads, int head_dim, int kv_head,
+                    int64_t t_begin, int64_t t_end, double scale, double *o, double *lse)
+{
+    for (int d = 0; d < head_dim; ++d)
+        o[d] = 0.0;
+    if (t_end <= t_begin) {
+        *lse = -INFINITY;
+        return 0;
+    }
+    int64_t n = t_end - t_begin;
+    double *s = (double *)malloc((size_t)n * sizeof(double));
+    if (!s)
+        return -2;
+    double m = -INFINITY;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = t_begin + i;
+        int64_t blk = bt_row[t / block_size];
+        if (blk < 0 || blk >= num_blocks) {
+            free(s);
+            return -1;
+        }
+        const uint8_t *k = k_cache + cache_row8(blk, t % block_size, kv_head, block_size,
+                                                num_kv_heads, head_dim);
+        double dot = 0.0;
+        for (int d = 0; d < head_dim; ++d)
+            dot += kfo_bf16_to_double(q_row[d]) * (kfo_e4m3_to_double(k[d]) * k_scale);
+        s[i] = scale * dot;
+        if (s[i] > m)
+            m = s[i];
+    }
+    double l = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t t = t_begin + i;
+        int64_t blk = bt_row[t / block_size];
+        const uint8_t *v = v_cache + cache_row8(blk, t % block_size, kv_head, block_size,
+                                                num_kv_heads, head_dim);
+        double p = exp(s[i] - m);
+        l += p;
+        for (int d = 0; d < head_dim; ++d)
+            o[d] += p * (kfo_e4m3_to_double(v[d]) * v_scale);
+    }
+    for (int d = 0; d < head_dim; ++d)
+        o[d] /= l;
+    *lse = m + log(l);
+    free(s);
+    return 0;
+}
+
+/* Partials of every split over an FP8 cache (see kfo_decode_partials);
+ * k_scale, v_scale are fp32 [num_kv_heads]. Single-threaded. */
+int kfo_decode_partials_fp8(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                            const float *k_scale, const float *v_scale,
+                            const int32_t *block_tables, int bt_stride, const int32_t *ctx_lens,
+                            int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int64_t num_blocks, double scale, int num_splits,
+                            int64_t max_context_len, const int32_t *rows, int64_t n_rows,
+                            double *o_part, double *lse_part)
+{
+    if (num_splits < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || block_size < 1)
+        return -4;
+    for (int b = 0; b < batch; ++b)
+        if (ctx_lens[b] < 0 || (int64_t)ctx_lens[b] > (int64_t)bt_stride * block_size ||
+            ctx_lens[b] > max_context_len)
+            return -3;
+    int G = num_q_heads / num_kv_heads;
+    if (!rows)
+        n_rows = (int64_t)batch * num_q_heads;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int b = rows ? rows[2 * r] : (int)(r / num_q_heads);
+        int h = rows ? rows[2 * r + 1] : (int)(r % num_q_heads);
+        const uint16_t *q_row = q + ((int64_t)b * num_q_heads + h) * head_dim;
+        const int32_t *bt_row = block_tables + (int64_t)b * bt_stride;
+        int kvh = h / G;
+        for (int s = 0; s < num_splits; ++s) {
+            int64_t t0, t1;
+            kfo_split_range(ctx_lens[b], block_size, num_splits, max_context_len, s, &t0, &t1);
+            int64_t slot = ((int64_t)s * batch + b) * num_q_heads + h;
+            int rc = kfo_partial_fp8(q_row, k_cache, v_cache, (double)k_scale[kvh],
+                                     (double)v_scale[kvh], bt_row, num_blocks, block_size,
+                                     num_kv_heads, head_dim, kvh, t0, t1, scale,
+                                     o_part + slot * head_dim, lse_part + slot);
+            if (rc != 0)
+                return rc;
+        }
+    }
+    return 0;
+}
+
+/*
+ * FP8 append: request b's new bf16 K/V rows are quantised (code of
+ * float(x) / scale[h], fp32 division) and written at position ctx_before[b]
+ * as kfo_append does. Returns the number of requests skipped.
+ */
+int kfo_append_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_new, const uint16_t *v_new,
+                   const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                   int bt_stride, const int32_t *ctx_before, int batch, int num_kv_heads,
+                   int head_dim, int block_size, int64_t num_blocks)
+{
+    int skipped = 0;
+    for (int b = 0; b < batch; ++b) {
+        int64_t p = ctx_before[b];
+        if (p < 0 || p >= (int64_t)bt_stride * block_size) {
+            ++skipped;
+            continue;
+        }
+        int64_t blk = block_tables[(int64_t)b * bt_stride + p / block_size];
+        if (blk < 0 || blk >= num_blocks) {
+            ++skipped;
+            continue;
+        }
+        for (int h = 0; h < num_kv_heads; ++h) {
+            int64_t dst = cache_row8(blk, p % block_size, h, block_size, num_kv_heads, head_dim);
+            int64_t src = ((int64_t)b * num_kv_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d) {
+                float kq = (float)kfo_bf16_to_double(k_new[src + d]) / k_scale[h];
+                float vq = (float)kfo_bf16_to_double(v_new[src + d]) / v_scale[h];
+                k_cache[dst + d] = kfo_e4m3_from_float(kq);
+                v_cache[dst + d] = kfo_e4m3_from_float(vq);
+            }
+        }
+    }
+    return skipped;
+}
+

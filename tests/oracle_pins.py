@@ -332,9 +332,119 @@ def pin_append_random(lib):
     assert skipped == 1 and np.array_equal(k3, k) and np.array_equal(v3, v)
 
 
+# ----------------------------------------------------------------------------
+# FP8 (E4M3) KV cache
+# ----------------------------------------------------------------------------
+
+def _torch_e4m3_table():
+    """Values of all 256 E4M3 codes decoded by torch's float8_e4m3fn (an
+    implementation independent of the oracle)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_e4m3_decode(lib):
+    # values fixed by the OCP E4M3 definition
+    spec = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x39: 1.125,
+            0x3F: 1.875, 0x40: 2.0, 0x7E: 448.0, 0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0}
+    for c, v in spec.items():
+        assert oracle.e4m3_to_f64(c, lib=lib) == v, hex(c)
+    assert math.isnan(oracle.e4m3_to_f64(0x7F, lib=lib)) and math.isnan(oracle.e4m3_to_f64(0xFF, lib=lib))
+    table = _torch_e4m3_table()
+    mine = np.array([oracle.e4m3_to_f64(c, lib=lib) for c in range(256)])
+    assert np.array_equal(np.isnan(mine), np.isnan(table))
+    fin = ~np.isnan(table)
+    assert np.array_equal(mine[fin], table[fin])
+
+
+def pin_e4m3_encode(lib):
+    """The code is the nearest finite E4M3 value (brute force over the table),
+    ties to the even code, saturating at +-448; NaN -> 0x7F."""
+    table = _torch_e4m3_table()
+    finite = [c for c in range(256) if not np.isnan(table[c])]
+    rng = np.random.default_rng(17)
+    xs = np.concatenate([rng.standard_normal(3000) * 4, rng.standard_normal(1000) * 200,
+                         rng.standard_normal(1000) * 0.01, rng.uniform(-460, 460, 500)]).astype(np.float32)
+    # exact halfway points between neighbouring positive codes, and their negatives
+    pos = sorted({table[c] for c in finite if table[c] > 0})
+    mids = np.array([(a + b) / 2 for a, b in zip(pos[:-1], pos[1:])], dtype=np.float64)
+    xs = np.concatenate([xs, mids.astype(np.float32), -mids.astype(np.float32)])
+    for x in xs:
+        xd = float(x)
+        if abs(xd) >= 448:
+            want = 0x7E | (0x80 if xd < 0 else 0)
+        else:
+            best = min(abs(table[c] - xd) for c in finite)
+            cands = [c for c in finite if abs(table[c] - xd) == best and (table[c] != 0 or c == (0x80 if np.signbit(xd) else 0))]
+            cands = [c for c in cands if (c & 0x80) == (0x80 if np.signbit(xd) else 0)] or cands
+            want = min(cands, key=lambda c: (c & 1, c))      # ties: even mantissa
+        assert oracle.e4m3_from_f32(x, lib=lib) == want, (xd, hex(want))
+    assert oracle.e4m3_from_f32(float("nan"), lib=lib) == 0x7F
+    assert oracle.e4m3_from_f32(float("inf"), lib=lib) == 0x7E
+    assert oracle.e4m3_from_f32(float("-inf"), lib=lib) == 0xFE
+    assert oracle.e4m3_from_f32(1e30, lib=lib) == 0x7E
+
+
+def _fp8_small(hq=4, hkv=2, d=16, bs=4, lengths=(5, 13, 22), seed=9):
+    w, inp = _small(batch=len(lengths), hq=hq, hkv=hkv, d=d, bs=bs, lengths=lengths, seed=seed)
+    rng = np.random.default_rng(seed)
+    nb = inp.k_cache.shape[0]
+    kc = rng.integers(0, 256, size=(nb, bs, hkv, d), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=(nb, bs, hkv, d), dtype=np.uint8)
+    # no NaN codes in the pool
+    kc[(kc & 0x7F) == 0x7F] ^= 1
+    vc[(vc & 0x7F) == 0x7F] ^= 1
+    ks = (2.0 ** -rng.integers(3, 7, size=hkv)).astype(np.float32)
+    vs = (2.0 ** -rng.integers(3, 7, size=hkv)).astype(np.float32)
+    return w, inp, kc, vc, ks, vs
+
+
+def pin_fp8_attention_is_dequantised_attention(lib):
+    """Attention over E4M3 codes equals the bf16 attention over a cache that
+    holds decode(code) * scale (exact in bf16 for power-of-two scales)."""
+    w, inp, kc, vc, ks, vs = _fp8_small()
+    q, _, _, bt, ctx = _arrays(inp)
+    table = _torch_e4m3_table()
+    kd = (table[kc] * ks[None, None, :, None]).astype(np.float32)
+    vd = (table[vc] * vs[None, None, :, None]).astype(np.float32)
+    out8, lse8 = oracle.attention_fp8(q, kc, vc, ks, vs, bt, ctx, w.scale, lib=lib)
+    out16, lse16 = oracle.attention(q, _bf16(kd), _bf16(vd), bt, ctx, w.scale, lib=lib)
+    np.testing.assert_allclose(out8, out16, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse8, lse16, rtol=1e-13, atol=1e-13)
+    # and the split partials merge back to it
+    o_p, l_p = oracle.decode_partials_fp8(q, kc, vc, ks, vs, bt, ctx, w.scale, 4, max_context_len=30, lib=lib)
+    m_o, m_l = oracle.merge_partials(o_p, l_p, lib=lib)
+    np.testing.assert_allclose(m_o, out8, rtol=0, atol=1e-12)
+
+
+def pin_fp8_append(lib):
+    """The new row's codes are E4M3(float(x) / scale) of its own KV head;
+    nothing else changes."""
+    w, inp, kc, vc, ks, vs = _fp8_small(lengths=(3, 4, 10))
+    _, _, _, bt, _ = _arrays(inp)
+    kn = _bf16(np.array([[[1.0, -2.0, 0.5, 288.0] * 4] * 2] * 3, np.float32))
+    vn = _bf16(np.array([[[0.25, 3.0, -0.125, 2.0 ** -10] * 4] * 2] * 3, np.float32))
+    ctx0 = inp.ctx_before.numpy()
+    k2, v2, skipped = oracle.append_fp8(kc, vc, kn, vn, ks, vs, bt, ctx0, lib=lib)
+    assert skipped == 0
+    ek, ev = kc.copy(), vc.copy()
+    knf, vnf = _widen(kn).astype(np.float32), _widen(vn).astype(np.float32)
+    for b in range(w.batch):
+        p = int(ctx0[b])
+        blk = bt[b, p // w.block_size]
+        for h in range(w.num_kv_heads):
+            for d in range(w.head_dim):
+                xk = knf[b, h, d] / np.float32(ks[h])
+                xv = vnf[b, h, d] / np.float32(vs[h])
+                ek[blk, p % w.block_size, h, d] = torch.tensor(min(max(float(xk), -448.0), 448.0)).to(torch.float8_e4m3fn).view(torch.uint8).item()
+                ev[blk, p % w.block_size, h, d] = torch.tensor(min(max(float(xv), -448.0), 448.0)).to(torch.float8_e4m3fn).view(torch.uint8).item()
+    assert np.array_equal(k2, ek) and np.array_equal(v2, ev)
+
+
 PINS = [
     pin_bf16_widening, pin_golden_two_token, pin_golden_gqa, pin_golden_merge, pin_golden_append,
     pin_context_len_one, pin_identical_keys, pin_scale_zero, pin_dominant_key, pin_head_mapping,
     pin_permutation_invariance, pin_split_ranges, pin_split_merge, pin_merge_properties,
     pin_shift_invariance, pin_scipy_brute_force, pin_append_random,
+    pin_e4m3_decode, pin_e4m3_encode, pin_fp8_attention_is_dequantised_attention, pin_fp8_append,
 ]

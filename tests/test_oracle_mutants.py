@@ -33,6 +33,13 @@ MUTANTS = {
     "bf16_widen_wrong_half": ("uint32_t u = ((uint32_t)bits) << 16;", "uint32_t u = ((uint32_t)bits) << 15;"),
     "score_sign": ("s[i] = scale * dot;", "s[i] = -scale * dot;"),
     "lse_base2": ("*lse = m + log(l);", "*lse = m + log2(l);"),
+    "e4m3_bias_off_by_one": ("v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
+    "e4m3_ties_away": ("if (frac > 0.5 || (frac == 0.5 && fmod(fl, 2.0) == 1.0))", "if (frac >= 0.5)"),
+    "e4m3_saturate_low": ("    if (a >= 448.0)\n        return sign | 0x7E;", "    if (a >= 440.0)\n        return sign | 0x7E;"),
+    "fp8_v_scale_dropped": ("o[d] += p * (kfo_e4m3_to_double(v[d]) * v_scale);", "o[d] += p * kfo_e4m3_to_double(v[d]);"),
+    "fp8_k_scale_is_v_scale": ("(double)k_scale[kvh],", "(double)v_scale[kvh],"),
+    "fp8_append_multiplies": ("float kq = (float)kfo_bf16_to_double(k_new[src + d]) / k_scale[h];",
+                              "float kq = (float)kfo_bf16_to_double(k_new[src + d]) * k_scale[h];"),
 }
 
 
@@ -40,6 +47,8 @@ MUTANTS = {
 def test_mutant_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
     src = open(SRC).read()
+    old = old.replace("\\n", "\n")
+    new = new.replace("\\n", "\n")
     assert src.count(old) >= 1, "mutation anchor not found: " + name
     mutated = src.replace(old, new)
     path = str(tmp_path / ("m_%s.c" % name))
