@@ -35,7 +35,7 @@ MUTANTS = {
     "lse_base2": ("*lse = m + log(l);", "*lse = m + log2(l);"),
     "e4m3_bias_off_by_one": ("v = ldexp(1.0 + m / 8.0, e - 7);", "v = ldexp(1.0 + m / 8.0, e - 8);"),
     "e4m3_ties_away": ("if (frac > 0.5 || (frac == 0.5 && fmod(fl, 2.0) == 1.0))", "if (frac >= 0.5)"),
-    "e4m3_saturate_low": ("    if (a >= 448.0)\n        return sign | 0x7E;", "    if (a >= 440.0)\n        return sign | 0x7E;"),
+    "e4m3_overflow_to_nan": ("    if (a >= 448.0)\n        return sign | 0x7E;", "    if (a >= 448.0)\n        return sign | 0x7F;"),
     "fp8_v_scale_dropped": ("o[d] += p * (kfo_e4m3_to_double(v[d]) * v_scale);", "o[d] += p * kfo_e4m3_to_double(v[d]);"),
     "fp8_k_scale_is_v_scale": ("(double)k_scale[kvh],", "(double)v_scale[kvh],"),
     "fp8_append_multiplies": ("float kq = (float)kfo_bf16_to_double(k_new[src + d]) / k_scale[h];",
