@@ -88,28 +88,33 @@ kf_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KF_OK : KF_ERR_CU
 
 // ----------------------------------------------------------------------------
 // Split planner: a model of the decode kernel's schedule. Work units are
-// (request, KV-head group, split) CTAs launched split-fastest; the hardware
-// hands each free slot the next CTA in launch order, which is simulated with
-// a heap of slot finish times. A CTA with tokens costs a fixed start-up plus
-// its bytes at the per-slot share of HBM bandwidth; an empty one costs its
-// zero-fill. The merge reads and writes S partial rows per output row.
+// (request, KV-head group, split) CTAs launched split-fastest. While CTAs are
+// still queued, every slot is busy and each CTA streams at the fair share of
+// HBM bandwidth; the hardware hands a freed slot the next CTA in launch order
+// (simulated with a heap of slot finish times). Once the queue is empty the
+// remaining CTAs drain, each at min(its own in-flight-bytes limit, bandwidth
+// / CTAs still running). A CTA pays a fixed start-up; an empty CTA only its
+// zero-fill; the merge reads and writes S partial rows per output row.
+// Constants were fitted to measured GB300 sweeps of split count on the five
+// workloads of the test suite.
 // ----------------------------------------------------------------------------
-constexpr double kHbmBytesPerUs = 6.0e6;   // sustained HBM bandwidth, bytes per microsecond
-constexpr double kCtaStartUs = 2.0;        // CTA start-up: table, q, first loads in flight
+constexpr double kHbmBytesPerUs = 7.0e6;   // sustained read bandwidth of the decode stream
+constexpr double kLatencyUs = 2.0;         // loaded DRAM round trip seen by one CTA's ring
+constexpr double kCtaStartUs = 1.5;        // CTA start-up: table, q, first loads in flight
 constexpr double kEmptyCtaUs = 0.25;       // CTA that only writes its empty partial
 constexpr double kLaunchUs = 3.0;          // one kernel launch
 
 double model_time(int S, int batch, int num_q_heads, int num_kv_heads, int head_dim,
                   int block_size, int64_t n_max, const int64_t *n_blocks, int heads_per_cta,
-                  int slots) {
+                  int slots, double ring_bytes) {
     const int64_t chunk = std::max<int64_t>(1, (n_max + S - 1) / S);
     const int groups = (num_kv_heads + heads_per_cta - 1) / heads_per_cta;
     const double bytes_per_block = 2.0 * block_size * heads_per_cta * head_dim * 2.0;
-    const double slot_bw = kHbmBytesPerUs / slots;
+    const double fair = kHbmBytesPerUs / slots;                // bytes/us per CTA, all slots busy
+    const double cap = std::max(fair, ring_bytes / kLatencyUs);  // one CTA alone
     std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
     for (int i = 0; i < slots; ++i) free_at.push(0.0);
-    double makespan = 0.0;
-    double empty_cost = 0.0;
+    double queue_empty_at = 0.0;
     int64_t empties = 0;
     for (int b = 0; b < batch; ++b) {
         const int64_t nb = n_blocks ? n_blocks[b] : n_max;
@@ -121,18 +126,31 @@ double model_time(int S, int batch, int num_q_heads, int num_kv_heads, int head_
                     ++empties;
                     continue;
                 }
-                const double t = kCtaStartUs + cnt * bytes_per_block / slot_bw;
                 const double start = free_at.top();
                 free_at.pop();
-                free_at.push(start + t);
-                makespan = std::max(makespan, start + t);
+                free_at.push(start + kCtaStartUs + cnt * bytes_per_block / fair);
+                queue_empty_at = start;
             }
         }
     }
-    empty_cost = empties * kEmptyCtaUs / slots;
+    // drain: remaining bytes of the CTAs still running when the queue empties
+    std::vector<double> rem;
+    while (!free_at.empty()) {
+        const double end = free_at.top();
+        free_at.pop();
+        if (end > queue_empty_at) rem.push_back((end - queue_empty_at) * fair);
+    }
+    std::sort(rem.begin(), rem.end());
+    double t = queue_empty_at, done = 0.0;
+    const size_t n = rem.size();
+    for (size_t i = 0; i < n; ++i) {
+        const double rate = std::min(cap, kHbmBytesPerUs / (double)(n - i));
+        t += (rem[i] - done) / rate;
+        done = rem[i];
+    }
     const double rows = (double)batch * num_q_heads;
     const double merge_bytes = rows * (S * (head_dim + 1) * 4.0 * 2.0 + head_dim * 4.0);
-    return makespan + empty_cost + kLaunchUs + merge_bytes / kHbmBytesPerUs + kLaunchUs;
+    return t + empties * kEmptyCtaUs / slots + kLaunchUs + merge_bytes / kHbmBytesPerUs + kLaunchUs;
 }
 
 }  // namespace
@@ -338,11 +356,13 @@ int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int h
         }
     }
     int hpc = 1, cps = 1;
+    double ring = 32768.0;
     if (decode_impl() == 1) {
         hpc = 1;
         cps = 8;
     } else {
         decode_tc_shape(num_kv_heads, head_dim, block_size, &hpc, &cps);
+        ring = decode_tc_ring_bytes(num_kv_heads, head_dim);
     }
     const int slots = num_sms * cps;
     static const int cands[] = {1,   2,   3,   4,   5,   6,   7,   8,   10,  12,  14,  16,
@@ -353,7 +373,7 @@ int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int h
     for (int S : cands) {
         if (S > n_max) break;
         const double t = model_time(S, batch, num_q_heads, num_kv_heads, head_dim, block_size,
-                                    n_max, nb.empty() ? nullptr : nb.data(), hpc, slots);
+                                    n_max, nb.empty() ? nullptr : nb.data(), hpc, slots, ring);
         if (t < best_t * 0.995) {  // prefer fewer splits unless clearly faster
             best_t = t;
             best = S;
