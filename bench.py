@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--path", default="auto", choices=["auto", "fused", "calls"],
                     help="fused: kf_decode_step (one launch); calls: append, attention, merge; "
                          "auto: fused for unsharded workloads with the tensor-core kernel")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
+                    help="cache element type (fp8 = E4M3 codes with per-KV-head scales)")
     ap.add_argument("--num-splits", type=int, default=None,
                     help="override the planner's split count (tuning sweeps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -156,7 +158,7 @@ def whole_job_gbs(bytes_per_rank: int, world: int, seconds_max: float) -> float:
 def kernel_source_digest() -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("kf_decode_tc.cu", "kf_internal.cuh"):
+    for f in ("kf_decode_tc.cuh", "kf_decode_tc.cu", "kf_internal.cuh"):
         with open(os.path.join(ROOT, "paged_kv_decode_kf_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -300,10 +302,14 @@ def run_ours(args):
     from paged_kv_decode_kf_gb300.step import DecodeStep
 
     w = wl.CONFIGS[args.workload]
+    if args.kv_dtype != "bf16":
+        w = wl.with_kv_dtype(w, args.kv_dtype)
     K = args.steps if args.steps is not None else default_steps(w.name)
     W = max(args.warmup, 3)
     dev = wl.make_inputs(w, "cuda:%d" % local)
     fused = args.path == "fused" or (args.path == "auto" and not w.shards and args.decode_kernel == "tc")
+    if w.kv_dtype == "fp8" and args.decode_kernel != "tc":
+        raise SystemExit("the FP8 cache is served by the tensor-core kernel only")
     step = DecodeStep(dev, num_splits=args.num_splits, fused=fused)
     kv_bytes = dev.kv_bytes()
     stream = torch.cuda.current_stream()
@@ -424,7 +430,8 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": ms, "us_per_step": ms * 1e3, "pct_of_hbm_peak": 100.0 * value / world / peak,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8 e4m3 KV, bf16 q",
             "accumulate": "f32", "data": "synthetic",
             "config": {"workload": w.name + ": " + w.description, "batch": w.batch,
                        "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,

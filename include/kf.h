@@ -237,6 +237,47 @@ kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, vo
                          kf_stream_t stream);
 
 /*
+ * FP8 (E4M3) KV cache: kf_append_kv_fp8, kf_paged_decode_attention_fp8,
+ * kf_decode_step_fp8.
+ *
+ * The decode posts of blog.lo0.es ("Quantised KV cache -- --kv-cache-dtype
+ * fp8") keep K/V in 8-bit floats with scales, halving the bytes a decode step
+ * reads. Here k_cache/v_cache hold OCP FP8 E4M3 codes (1 byte per element,
+ * same [num_blocks, block_size, num_kv_heads, head_dim] layout) and
+ * k_scale/v_scale are fp32 [num_kv_heads] device arrays: element value =
+ * e4m3(code) * scale of its KV head. The calls take the same arguments as
+ * their bf16 counterparts plus the two scale arrays and compute the same
+ * thing on the dequantised values; q, k_new and v_new stay bf16. The append
+ * (and the fused step's append) stores code = E4M3 round-to-nearest-even,
+ * saturating to +-448, of the fp32 quotient float(x) / scale. The decode
+ * kernel widens the codes to bf16 exactly and accumulates in fp32.
+ * Host errors as the bf16 calls, plus null scales -> KF_ERR_INVALID.
+ */
+kf_status kf_append_kv_fp8(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                           const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                           int bt_stride, const int32_t *context_lens_before, int batch,
+                           int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                           kf_stream_t stream);
+
+kf_status kf_paged_decode_attention_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                        const float *k_scale, const float *v_scale,
+                                        const int32_t *block_tables, int bt_stride,
+                                        const int32_t *context_lens, int max_context_len,
+                                        int batch, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int64_t num_blocks,
+                                        float scale, int num_splits, float *out_partial,
+                                        float *lse_partial, kf_stream_t stream);
+
+kf_status kf_decode_step_fp8(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                             void *v_cache, const float *k_scale, const float *v_scale,
+                             const int32_t *block_tables, int bt_stride,
+                             const int32_t *context_lens_before, int max_context_len, int batch,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             int64_t num_blocks, float scale, int num_splits, void *workspace,
+                             size_t workspace_bytes, void *out, kf_dtype out_dtype,
+                             float *lse_out, kf_stream_t stream);
+
+/*
  * kf_decode_step_static -- kf_decode_step without a caller-provided workspace,
  * for callers that may not allocate device memory.
  *

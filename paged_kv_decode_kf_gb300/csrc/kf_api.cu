@@ -98,8 +98,8 @@ kf_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KF_OK : KF_ERR_CU
 // Constants were fitted to measured GB300 sweeps of split count on the five
 // workloads of the test suite.
 // ----------------------------------------------------------------------------
-constexpr double kHbmBytesPerUs = 7.0e6;   // sustained read bandwidth of the decode stream
-constexpr double kLatencyUs = 2.0;         // loaded DRAM round trip seen by one CTA's ring
+constexpr double kHbmBytesPerUs = 7.2e6;   // sustained read bandwidth of the decode stream
+constexpr double kLatencyUs = 3.0;         // loaded DRAM round trip seen by one CTA's ring
 constexpr double kCtaStartUs = 1.5;        // CTA start-up: table, q, first loads in flight
 constexpr double kEmptyCtaUs = 0.25;       // CTA that only writes its empty partial
 constexpr double kLaunchUs = 3.0;          // one kernel launch
@@ -202,19 +202,46 @@ kf_status kf_append_kv(const void *k_new, const void *v_new, void *k_cache, void
         dev->err, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-kf_status kf_paged_decode_attention(const void *q, const void *k_cache, const void *v_cache,
-                                    const int32_t *block_tables, int bt_stride,
-                                    const int32_t *context_lens, int max_context_len, int batch,
-                                    int num_q_heads, int num_kv_heads, int head_dim,
-                                    int block_size, int64_t num_blocks, float scale,
-                                    int num_splits, float *out_partial, float *lse_partial,
-                                    kf_stream_t stream) {
+kf_status kf_append_kv_fp8(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                           const float *k_scale, const float *v_scale, const int32_t *block_tables,
+                           int bt_stride, const int32_t *context_lens_before, int batch,
+                           int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                           kf_stream_t stream) {
+    if (batch < 0 || num_kv_heads < 1 || bt_stride < 1 || num_blocks < 1 || head_dim < 1 ||
+        block_size < 1)
+        return KF_ERR_INVALID;
+    if (batch == 0) return KF_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !block_tables || !context_lens_before ||
+        !k_scale || !v_scale)
+        return KF_ERR_INVALID;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+        return KF_ERR_INVALID;
+    if (!supported_dims(head_dim, block_size)) return KF_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return KF_ERR_CUDA;
+    return from_cuda(launch_append_fp8(
+        static_cast<const uint16_t *>(k_new), static_cast<const uint16_t *>(v_new),
+        static_cast<uint8_t *>(k_cache), static_cast<uint8_t *>(v_cache), k_scale, v_scale,
+        block_tables, bt_stride, context_lens_before, batch, num_kv_heads, head_dim, block_size,
+        num_blocks, dev->err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace {
+
+kf_status attention_impl(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, int bt_stride, const int32_t *context_lens,
+                         int max_context_len, int batch, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, int64_t num_blocks, float scale,
+                         int num_splits, float *out_partial, float *lse_partial,
+                         const float *k_scale, const float *v_scale, bool kv8, kf_stream_t stream) {
     if (batch < 0 || num_splits < 1 || bt_stride < 1 || num_blocks < 1 || max_context_len < 0 ||
         num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || !isfinite(scale))
         return KF_ERR_INVALID;
     if (batch == 0) return KF_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out_partial ||
-        !lse_partial)
+        !lse_partial || (kv8 && (!k_scale || !v_scale)))
         return KF_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out_partial))
         return KF_ERR_INVALID;
@@ -245,11 +272,44 @@ kf_status kf_paged_decode_attention(const void *q, const void *k_cache, const vo
     const int64_t n_max = ((int64_t)max_context_len + block_size - 1) / block_size;
     p.chunk_blocks = (int)std::max<int64_t>(1, (n_max + num_splits - 1) / num_splits);
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.k_scale = kv8 ? k_scale : nullptr;
+    p.v_scale = kv8 ? v_scale : nullptr;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (decode_impl() == 1) return from_cuda(launch_decode_simt(p, st));
+    if (!kv8 && decode_impl() == 1) return from_cuda(launch_decode_simt(p, st));
     void *fn = encode_fn();
     if (!fn) return KF_ERR_CUDA;
-    return from_cuda(launch_decode_tc(p, st, fn));
+    return from_cuda(kv8 ? launch_decode_tc_fp8(p, st, fn) : launch_decode_tc(p, st, fn));
+}
+
+}  // namespace
+
+extern "C" {
+
+kf_status kf_paged_decode_attention(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_tables, int bt_stride,
+                                    const int32_t *context_lens, int max_context_len, int batch,
+                                    int num_q_heads, int num_kv_heads, int head_dim,
+                                    int block_size, int64_t num_blocks, float scale,
+                                    int num_splits, float *out_partial, float *lse_partial,
+                                    kf_stream_t stream) {
+    return attention_impl(q, k_cache, v_cache, block_tables, bt_stride, context_lens,
+                          max_context_len, batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, scale, num_splits, out_partial, lse_partial, nullptr, nullptr,
+                          false, stream);
+}
+
+kf_status kf_paged_decode_attention_fp8(const void *q, const void *k_cache, const void *v_cache,
+                                        const float *k_scale, const float *v_scale,
+                                        const int32_t *block_tables, int bt_stride,
+                                        const int32_t *context_lens, int max_context_len,
+                                        int batch, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int64_t num_blocks,
+                                        float scale, int num_splits, float *out_partial,
+                                        float *lse_partial, kf_stream_t stream) {
+    return attention_impl(q, k_cache, v_cache, block_tables, bt_stride, context_lens,
+                          max_context_len, batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                          num_blocks, scale, num_splits, out_partial, lse_partial, k_scale,
+                          v_scale, true, stream);
 }
 
 size_t kf_decode_step_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
@@ -261,20 +321,24 @@ size_t kf_decode_step_workspace_size(int batch, int num_q_heads, int num_kv_head
            al((size_t)batch * num_kv_heads * 4);
 }
 
-kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache,
-                         void *v_cache, const int32_t *block_tables, int bt_stride,
-                         const int32_t *context_lens_before, int max_context_len, int batch,
-                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                         int64_t num_blocks, float scale, int num_splits, void *workspace,
-                         size_t workspace_bytes, void *out, kf_dtype out_dtype, float *lse_out,
-                         kf_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+kf_status step_impl(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                    void *v_cache, const int32_t *block_tables, int bt_stride,
+                    const int32_t *context_lens_before, int max_context_len, int batch,
+                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                    int64_t num_blocks, float scale, int num_splits, void *workspace,
+                    size_t workspace_bytes, void *out, kf_dtype out_dtype, float *lse_out,
+                    const float *k_scale, const float *v_scale, bool kv8, kf_stream_t stream) {
     if (batch < 0 || num_splits < 1 || bt_stride < 1 || num_blocks < 1 || max_context_len < 0 ||
         num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || !isfinite(scale) ||
         (out_dtype != KF_BF16 && out_dtype != KF_F32))
         return KF_ERR_INVALID;
     if (batch == 0) return KF_OK;
     if (!q || !k_new || !v_new || !k_cache || !v_cache || !block_tables || !context_lens_before ||
-        !out)
+        !out || (kv8 && (!k_scale || !v_scale)))
         return KF_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
         !aligned16(v_cache) || !aligned16(out))
@@ -288,9 +352,9 @@ kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, vo
         return KF_ERR_INVALID;
     // the last CTA of a group merges in its shared-memory ring: S x rows x 4 bytes must fit
     int hpc = 1, cps = 1;
-    decode_tc_shape(num_kv_heads, head_dim, block_size, &hpc, &cps);
+    decode_tc_shape(num_kv_heads, head_dim, block_size, kv8, &hpc, &cps);
     const int R = hpc * (num_q_heads / num_kv_heads);
-    if ((int64_t)num_splits * R * 4 + 8 * R > decode_tc_ring_bytes(num_kv_heads, head_dim))
+    if ((int64_t)num_splits * R * 4 + 8 * R > decode_tc_ring_bytes(num_kv_heads, head_dim, kv8))
         return KF_ERR_UNSUPPORTED;
     DeviceInfo *dev = nullptr;
     if (device_info(&dev) != cudaSuccess) return KF_ERR_CUDA;
@@ -316,6 +380,8 @@ kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, vo
     const int64_t n_max = ((int64_t)max_context_len + block_size - 1) / block_size;
     p.chunk_blocks = (int)std::max<int64_t>(1, (n_max + num_splits - 1) / num_splits);
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.k_scale = kv8 ? k_scale : nullptr;
+    p.v_scale = kv8 ? v_scale : nullptr;
 
     const size_t rows = (size_t)batch * num_q_heads;
     const auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
@@ -323,8 +389,8 @@ kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, vo
     StepArgs a;
     a.k_new = static_cast<const uint16_t *>(k_new);
     a.v_new = static_cast<const uint16_t *>(v_new);
-    a.k_cache = static_cast<uint16_t *>(k_cache);
-    a.v_cache = static_cast<uint16_t *>(v_cache);
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
     a.ws_o = num_splits > 1 ? reinterpret_cast<float *>(ws) : nullptr;
     a.ws_lse = num_splits > 1 ? reinterpret_cast<float *>(ws + al((size_t)num_splits * rows * head_dim * 4)) : nullptr;
     a.counters = num_splits > 1 ? reinterpret_cast<unsigned int *>(
@@ -336,7 +402,40 @@ kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, vo
     a.out_dtype = (int)out_dtype;
     void *fn = encode_fn();
     if (!fn) return KF_ERR_CUDA;
-    return from_cuda(launch_decode_step_tc(p, a, reinterpret_cast<cudaStream_t>(stream), fn));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return from_cuda(kv8 ? launch_decode_step_tc_fp8(p, a, st, fn) : launch_decode_step_tc(p, a, st, fn));
+}
+
+
+}  // namespace
+
+extern "C" {
+
+kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                         void *v_cache, const int32_t *block_tables, int bt_stride,
+                         const int32_t *context_lens_before, int max_context_len, int batch,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int64_t num_blocks, float scale, int num_splits, void *workspace,
+                         size_t workspace_bytes, void *out, kf_dtype out_dtype, float *lse_out,
+                         kf_stream_t stream) {
+    return step_impl(q, k_new, v_new, k_cache, v_cache, block_tables, bt_stride,
+                     context_lens_before, max_context_len, batch, num_q_heads, num_kv_heads,
+                     head_dim, block_size, num_blocks, scale, num_splits, workspace,
+                     workspace_bytes, out, out_dtype, lse_out, nullptr, nullptr, false, stream);
+}
+
+kf_status kf_decode_step_fp8(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                             void *v_cache, const float *k_scale, const float *v_scale,
+                             const int32_t *block_tables, int bt_stride,
+                             const int32_t *context_lens_before, int max_context_len, int batch,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             int64_t num_blocks, float scale, int num_splits, void *workspace,
+                             size_t workspace_bytes, void *out, kf_dtype out_dtype,
+                             float *lse_out, kf_stream_t stream) {
+    return step_impl(q, k_new, v_new, k_cache, v_cache, block_tables, bt_stride,
+                     context_lens_before, max_context_len, batch, num_q_heads, num_kv_heads,
+                     head_dim, block_size, num_blocks, scale, num_splits, workspace,
+                     workspace_bytes, out, out_dtype, lse_out, k_scale, v_scale, true, stream);
 }
 
 int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int head_dim,
@@ -361,8 +460,8 @@ int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int h
         hpc = 1;
         cps = 8;
     } else {
-        decode_tc_shape(num_kv_heads, head_dim, block_size, &hpc, &cps);
-        ring = decode_tc_ring_bytes(num_kv_heads, head_dim);
+        decode_tc_shape(num_kv_heads, head_dim, block_size, false, &hpc, &cps);
+        ring = decode_tc_ring_bytes(num_kv_heads, head_dim, false);
     }
     const int slots = num_sms * cps;
     static const int cands[] = {1,   2,   3,   4,   5,   6,   7,   8,   10,  12,  14,  16,

@@ -30,14 +30,16 @@ struct DecodeParams {
     int num_splits;
     int chunk_blocks;         // blocks per split: max(1, ceil(ceil(max_ctx/bs)/S))
     float scale_log2;         // scale * log2(e)
+    const float *k_scale;     // FP8 caches: per-KV-head dequantisation scales, else null
+    const float *v_scale;
 };
 
 // Extra arguments of the single-launch decode step (append + attention + merge).
 struct StepArgs {
     const uint16_t *k_new;   // bf16 [B, Hkv, D]
     const uint16_t *v_new;
-    uint16_t *k_cache;       // written at each request's new position
-    uint16_t *v_cache;
+    void *k_cache;           // written at each request's new position (bf16 or E4M3)
+    void *v_cache;
     float *ws_o;             // workspace partials [S, B, Hq, D]
     float *ws_lse;           // workspace lse [S, B, Hq]
     unsigned int *counters;  // workspace [B, Hkv], zero between steps
@@ -51,11 +53,14 @@ cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream, void *encode_fn);
 cudaError_t launch_decode_step_tc(const DecodeParams &p, const StepArgs &a, cudaStream_t stream,
                                   void *encode_fn);
+cudaError_t launch_decode_tc_fp8(const DecodeParams &p, cudaStream_t stream, void *encode_fn);
+cudaError_t launch_decode_step_tc_fp8(const DecodeParams &p, const StepArgs &a, cudaStream_t stream,
+                                      void *encode_fn);
 // Bytes of the tensor-core kernel's shared-memory ring (the fused merge reuses it).
-int decode_tc_ring_bytes(int num_kv_heads, int head_dim);
+int decode_tc_ring_bytes(int num_kv_heads, int head_dim, bool kv8);
 // Largest number of resident CTAs per SM and KV heads per CTA the tensor-core
 // kernel uses for this shape (for the split planner).
-void decode_tc_shape(int num_kv_heads, int head_dim, int block_size, int *heads_per_cta,
+void decode_tc_shape(int num_kv_heads, int head_dim, int block_size, bool kv8, int *heads_per_cta,
                      int *ctas_per_sm);
 
 cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t *k_cache,
@@ -63,6 +68,12 @@ cudaError_t launch_append(const uint16_t *k_new, const uint16_t *v_new, uint16_t
                           const int32_t *ctx_before, int batch, int num_kv_heads, int head_dim,
                           int block_size, int64_t num_blocks, unsigned int *err,
                           cudaStream_t stream);
+
+cudaError_t launch_append_fp8(const uint16_t *k_new, const uint16_t *v_new, uint8_t *k_cache,
+                              uint8_t *v_cache, const float *k_scale, const float *v_scale,
+                              const int32_t *block_tables, int bt_stride, const int32_t *ctx_before,
+                              int batch, int num_kv_heads, int head_dim, int block_size,
+                              int64_t num_blocks, unsigned int *err, cudaStream_t stream);
 
 cudaError_t launch_merge(const float *out_partial, const float *lse_partial, int num_partials,
                          int batch, int num_q_heads, int head_dim, void *out, int out_dtype,

@@ -53,6 +53,15 @@ _lib.kf_decode_step_static.restype = _i32
 _lib.kf_decode_step_static.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                        _i32, _i32, _i64, _f32, _i32, _vp, _i32, _vp, _vp]
 KF_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
+_lib.kf_append_kv_fp8.restype = _i32
+_lib.kf_append_kv_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i64, _vp]
+_lib.kf_paged_decode_attention_fp8.restype = _i32
+_lib.kf_paged_decode_attention_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
+                                               _i32, _i32, _i32, _i64, _f32, _i32, _vp, _vp, _vp]
+_lib.kf_decode_step_fp8.restype = _i32
+_lib.kf_decode_step_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32,
+                                    _i32, _i32, _i32, _i64, _f32, _i32, _vp, ctypes.c_size_t, _vp, _i32, _vp,
+                                    _vp]
 _lib.kf_get_device_error.restype = _i32
 _lib.kf_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), _vp]
 _lib.kf_status_string.restype = ctypes.c_char_p
@@ -242,6 +251,77 @@ def kf_decode_step_static(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Ten
         bs, nb, float(scale), int(num_splits), _dev(out, out.dtype, "out"), code,
         None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
         "kf_decode_step_static")
+
+
+def _dev8(t: torch.Tensor, name: str) -> int:
+    """An FP8 E4M3 cache: uint8 codes or torch.float8_e4m3fn."""
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise ValueError("%s must be uint8 E4M3 codes or float8_e4m3fn, got %s" % (name, t.dtype))
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    return t.data_ptr()
+
+
+def kf_append_kv_fp8(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables,
+                     context_lens_before, stream=None) -> None:
+    """Quantise and write each request's new K/V row into E4M3 caches."""
+    nb, bs, hkv, d = k_cache.shape
+    B = block_tables.shape[0]
+    _check(_lib.kf_append_kv_fp8(
+        _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev8(k_cache, "k_cache"), _dev8(v_cache, "v_cache"), _dev(k_scale, torch.float32, "k_scale"),
+        _dev(v_scale, torch.float32, "v_scale"), _dev(block_tables, torch.int32, "block_tables"),
+        block_tables.shape[1], _dev(context_lens_before, torch.int32, "context_lens_before"), B, hkv, d,
+        bs, nb, _stream(stream)), "kf_append_kv_fp8")
+
+
+def kf_paged_decode_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                                  max_context_len: int, scale: float, num_splits: int,
+                                  out_partial=None, lse_partial=None, stream=None):
+    """Split-KV decode attention over E4M3 caches; returns (out_partial, lse_partial)."""
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if out_partial is None:
+        out_partial = torch.empty((num_splits, B, hq, d), dtype=torch.float32, device=q.device)
+    if lse_partial is None:
+        lse_partial = torch.empty((num_splits, B, hq), dtype=torch.float32, device=q.device)
+    _check(_lib.kf_paged_decode_attention_fp8(
+        _dev(q, torch.bfloat16, "q"), _dev8(k_cache, "k_cache"), _dev8(v_cache, "v_cache"),
+        _dev(k_scale, torch.float32, "k_scale"), _dev(v_scale, torch.float32, "v_scale"),
+        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, torch.int32, "context_lens"), int(max_context_len), B, hq, hkv, d, bs, nb,
+        float(scale), int(num_splits), _dev(out_partial, torch.float32, "out_partial"),
+        _dev(lse_partial, torch.float32, "lse_partial"), _stream(stream)), "kf_paged_decode_attention_fp8")
+    return out_partial, lse_partial
+
+
+def kf_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables,
+                       context_lens_before, max_context_len: int, scale: float, num_splits: int,
+                       workspace=None, out=None, out_dtype=torch.float32, lse_out=None, want_lse=True,
+                       stream=None):
+    """Single-launch decode step over E4M3 caches; returns (out, lse)."""
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
+    code = {torch.float32: KF_F32, torch.bfloat16: KF_BF16}.get(out.dtype)
+    if code is None:
+        raise ValueError("out must be float32 or bfloat16")
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+    if workspace is None and num_splits > 1:
+        raise ValueError("num_splits > 1 needs a workspace (make_workspace)")
+    _check(_lib.kf_decode_step_fp8(
+        _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev8(k_cache, "k_cache"), _dev8(v_cache, "v_cache"), _dev(k_scale, torch.float32, "k_scale"),
+        _dev(v_scale, torch.float32, "v_scale"), _dev(block_tables, torch.int32, "block_tables"),
+        block_tables.shape[1], _dev(context_lens_before, torch.int32, "context_lens_before"),
+        int(max_context_len), B, hq, hkv, d, bs, nb, float(scale), int(num_splits),
+        None if workspace is None else _dev(workspace, torch.uint8, "workspace"),
+        0 if workspace is None else workspace.numel(), _dev(out, out.dtype, "out"), code,
+        None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
+        "kf_decode_step_fp8")
+    return out, lse_out
 
 
 def kf_get_device_error(stream=None) -> int:

@@ -57,8 +57,16 @@ class DecodeStep:
         return kf.kf_choose_num_splits(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                        w.block_size, max_ctx, ctx_lens.cpu().numpy().astype(np.int32))
 
+    @property
+    def fp8(self) -> bool:
+        return self.w.kv_dtype == "fp8"
+
     def append(self, stream=None) -> None:
         i = self.inp
+        if self.fp8:
+            bt, ctx = (i.tail_tables, i.tail_ctx_before) if self.w.shards else (i.block_tables, i.ctx_before)
+            kf.kf_append_kv_fp8(i.k_new, i.v_new, i.k_cache, i.v_cache, i.k_scale, i.v_scale, bt, ctx, stream)
+            return
         if self.w.shards:
             kf.kf_append_kv(i.k_new, i.v_new, i.k_cache, i.v_cache, i.tail_tables, i.tail_ctx_before, stream)
         else:
@@ -67,15 +75,25 @@ class DecodeStep:
     def attention(self, stream=None) -> None:
         i, S = self.inp, self.num_splits
         for j, (bt, ctx, max_ctx) in enumerate(self.views):
-            kf.kf_paged_decode_attention(i.q, i.k_cache, i.v_cache, bt, ctx, max_ctx, self.w.scale, S,
-                                         self.out_partial[j * S:(j + 1) * S],
-                                         self.lse_partial[j * S:(j + 1) * S], stream)
+            if self.fp8:
+                kf.kf_paged_decode_attention_fp8(i.q, i.k_cache, i.v_cache, i.k_scale, i.v_scale, bt, ctx,
+                                                 max_ctx, self.w.scale, S, self.out_partial[j * S:(j + 1) * S],
+                                                 self.lse_partial[j * S:(j + 1) * S], stream)
+            else:
+                kf.kf_paged_decode_attention(i.q, i.k_cache, i.v_cache, bt, ctx, max_ctx, self.w.scale, S,
+                                             self.out_partial[j * S:(j + 1) * S],
+                                             self.lse_partial[j * S:(j + 1) * S], stream)
 
     def merge(self, stream=None) -> None:
         kf.kf_merge_partials(self.out_partial, self.lse_partial, self.out, lse_out=self.lse, stream=stream)
 
     def step_fused(self, stream=None) -> None:
         i = self.inp
+        if self.fp8:
+            kf.kf_decode_step_fp8(i.q, i.k_new, i.v_new, i.k_cache, i.v_cache, i.k_scale, i.v_scale,
+                                  i.block_tables, i.ctx_before, self.max_ctx, self.w.scale, self.num_splits,
+                                  self.workspace, self.out, lse_out=self.lse, stream=stream)
+            return
         kf.kf_decode_step(i.q, i.k_new, i.v_new, i.k_cache, i.v_cache, i.block_tables, i.ctx_before,
                           self.max_ctx, self.w.scale, self.num_splits, self.workspace, self.out,
                           lse_out=self.lse, stream=stream)

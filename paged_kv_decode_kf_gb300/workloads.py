@@ -116,6 +116,7 @@ class Workload:
     num_splits: tuple = (0,)       # 0 = library's choice
     shards: int = 0                # >0: KV spread over this many token-range shards
     description: str = ""
+    kv_dtype: str = "bf16"         # "bf16" or "fp8" (E4M3 codes with per-KV-head scales)
 
     @property
     def group(self) -> int:
@@ -126,8 +127,8 @@ class Workload:
         return 1.0 / math.sqrt(self.head_dim)
 
     def kv_bytes_per_token(self) -> int:
-        """K and V bytes of one token over all KV heads (bf16)."""
-        return 2 * self.num_kv_heads * self.head_dim * 2
+        """K and V bytes of one token over all KV heads."""
+        return 2 * self.num_kv_heads * self.head_dim * (1 if self.kv_dtype == "fp8" else 2)
 
 
 CONFIGS = {
@@ -163,7 +164,8 @@ CONFIG_ORDER = ("tiny", "llama8b", "longctx", "shard4", "ragged")
 
 
 def scaled(w: Workload, *, batch: Optional[int] = None, lengths=None, name=None,
-           seed: Optional[int] = None, spare_blocks: Optional[int] = None) -> Workload:
+           seed: Optional[int] = None, spare_blocks: Optional[int] = None,
+           kv_dtype: Optional[str] = None) -> Workload:
     """The same heads/dims/block size as `w` with another batch or length mix
     (used for oracle-sized parity cases)."""
     return Workload(
@@ -172,7 +174,25 @@ def scaled(w: Workload, *, batch: Optional[int] = None, lengths=None, name=None,
         block_size=w.block_size, lengths=lengths if lengths is not None else w.lengths,
         seed=seed if seed is not None else w.seed + 7919,
         spare_blocks=w.spare_blocks if spare_blocks is None else spare_blocks,
-        num_splits=w.num_splits, shards=w.shards, description=w.description)
+        num_splits=w.num_splits, shards=w.shards, description=w.description,
+        kv_dtype=kv_dtype or w.kv_dtype)
+
+
+def with_kv_dtype(w: Workload, kv_dtype: str) -> Workload:
+    """`w` with another cache element type (same lengths, tables and seed)."""
+    return Workload(name=w.name, batch=w.batch, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                    head_dim=w.head_dim, block_size=w.block_size, lengths=w.lengths, seed=w.seed,
+                    spare_blocks=w.spare_blocks, num_splits=w.num_splits, shards=w.shards,
+                    description=w.description + ("" if kv_dtype == "bf16" else ", FP8 E4M3 KV cache"),
+                    kv_dtype=kv_dtype)
+
+
+def fp8_scales(num_kv_heads: int):
+    """Per-KV-head K and V scales of the FP8 workloads: powers of two 2^-(4..6),
+    so N(0,1) data sits well inside E4M3's +-448 after division."""
+    k = np.array([2.0 ** -(4 + h % 3) for h in range(num_kv_heads)], dtype=np.float32)
+    v = np.array([2.0 ** -(4 + (h + 1) % 3) for h in range(num_kv_heads)], dtype=np.float32)
+    return k, v
 
 
 # ----------------------------------------------------------------------------
@@ -195,6 +215,9 @@ class DecodeInputs:
     k_new: torch.Tensor
     v_new: torch.Tensor
     block_tables: torch.Tensor
+    # ... FP8 caches: k_cache/v_cache are uint8 E4M3 codes, with these scales
+    k_scale: Optional[torch.Tensor] = field(default=None, kw_only=True)
+    v_scale: Optional[torch.Tensor] = field(default=None, kw_only=True)
     ctx_before: torch.Tensor
     ctx_after: torch.Tensor
     num_blocks: int
@@ -221,7 +244,8 @@ class DecodeInputs:
             k_new=mv(self.k_new), v_new=mv(self.v_new), block_tables=mv(self.block_tables),
             ctx_before=mv(self.ctx_before), ctx_after=mv(self.ctx_after), num_blocks=self.num_blocks,
             shards=[ShardView(mv(s.block_tables), mv(s.ctx_after), s.first_block) for s in self.shards],
-            tail_tables=mv(self.tail_tables), tail_ctx_before=mv(self.tail_ctx_before))
+            tail_tables=mv(self.tail_tables), tail_ctx_before=mv(self.tail_ctx_before),
+            k_scale=mv(self.k_scale), v_scale=mv(self.v_scale))
 
 
 def _bf16_normal(shape, gen: torch.Generator, device) -> torch.Tensor:
@@ -317,11 +341,20 @@ def make_inputs(w: Workload, device="cpu", lengths: Optional[Sequence[int]] = No
     v_cache = _bf16_normal((NB, bs, Hkv, D), gen, dev)
     k_new = _bf16_normal((B, Hkv, D), gen, dev)
     v_new = _bf16_normal((B, Hkv, D), gen, dev)
+    k_scale = v_scale = None
+    if w.kv_dtype == "fp8":
+        # E4M3 codes of the same N(0,1) draws divided by the per-head scales,
+        # converted by torch's float8_e4m3fn cast
+        ks, vs = fp8_scales(Hkv)
+        k_scale = torch.from_numpy(ks).to(dev)
+        v_scale = torch.from_numpy(vs).to(dev)
+        k_cache = (k_cache.float() / k_scale.view(1, 1, Hkv, 1)).to(torch.float8_e4m3fn).view(torch.uint8)
+        v_cache = (v_cache.float() / v_scale.view(1, 1, Hkv, 1)).to(torch.float8_e4m3fn).view(torch.uint8)
     i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
     inp = DecodeInputs(
         workload=w, q=q, k_cache=k_cache, v_cache=v_cache, k_new=k_new, v_new=v_new,
         block_tables=i32(lay.block_tables), ctx_before=i32(lay.ctx_before),
-        ctx_after=i32(lay.ctx_after), num_blocks=NB)
+        ctx_after=i32(lay.ctx_after), num_blocks=NB, k_scale=k_scale, v_scale=v_scale)
     for tab, ctx, first in zip(lay.shard_tables, lay.shard_ctx_after, lay.shard_first_block):
         inp.shards.append(ShardView(i32(tab), i32(ctx), first))
     if lay.tail_tables is not None:
