@@ -161,6 +161,15 @@ int kf_choose_num_splits(int batch, int num_q_heads, int num_kv_heads, int head_
                          int device);
 
 /*
+ * kf_choose_num_splits_fp8 -- the plan for the FP8-cache calls
+ * (kf_paged_decode_attention_fp8, kf_decode_step_fp8) on a GPU with `num_sms`
+ * SMs: same model with one-byte elements and the FP8 kernel's shape.
+ */
+int kf_choose_num_splits_fp8(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_context_len,
+                             const int32_t *context_lens_host, int num_sms);
+
+/*
  * kf_choose_num_splits_for -- the same plan for a GPU with `num_sms` SMs,
  * without touching any device (for planning on the host ahead of time).
  * The paged-decode pages give no split rule; this is the library's own

@@ -106,10 +106,10 @@ constexpr double kLaunchUs = 3.0;          // one kernel launch
 
 double model_time(int S, int batch, int num_q_heads, int num_kv_heads, int head_dim,
                   int block_size, int64_t n_max, const int64_t *n_blocks, int heads_per_cta,
-                  int slots, double ring_bytes) {
+                  int slots, double ring_bytes, double elem_bytes) {
     const int64_t chunk = std::max<int64_t>(1, (n_max + S - 1) / S);
     const int groups = (num_kv_heads + heads_per_cta - 1) / heads_per_cta;
-    const double bytes_per_block = 2.0 * block_size * heads_per_cta * head_dim * 2.0;
+    const double bytes_per_block = 2.0 * block_size * heads_per_cta * head_dim * elem_bytes;
     const double fair = kHbmBytesPerUs / slots;                // bytes/us per CTA, all slots busy
     const double cap = std::max(fair, ring_bytes / kLatencyUs);  // one CTA alone
     std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
@@ -438,9 +438,12 @@ kf_status kf_decode_step_fp8(const void *q, const void *k_new, const void *v_new
                      workspace_bytes, out, out_dtype, lse_out, k_scale, v_scale, true, stream);
 }
 
-int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int head_dim,
-                             int block_size, int max_context_len,
-                             const int32_t *context_lens_host, int num_sms) {
+}  // extern "C"
+
+namespace {
+
+int choose_splits(int batch, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                  int max_context_len, const int32_t *context_lens_host, int num_sms, bool kv8) {
     if (batch < 1 || max_context_len < 0 || num_sms < 1 || block_size < 1 ||
         !supported_dims(head_dim, block_size) || !supported_group(num_q_heads, num_kv_heads))
         return -1;
@@ -456,12 +459,12 @@ int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int h
     }
     int hpc = 1, cps = 1;
     double ring = 32768.0;
-    if (decode_impl() == 1) {
+    if (!kv8 && decode_impl() == 1) {
         hpc = 1;
         cps = 8;
     } else {
-        decode_tc_shape(num_kv_heads, head_dim, block_size, false, &hpc, &cps);
-        ring = decode_tc_ring_bytes(num_kv_heads, head_dim, false);
+        decode_tc_shape(num_kv_heads, head_dim, block_size, kv8, &hpc, &cps);
+        ring = decode_tc_ring_bytes(num_kv_heads, head_dim, kv8);
     }
     const int slots = num_sms * cps;
     static const int cands[] = {1,   2,   3,   4,   5,   6,   7,   8,   10,  12,  14,  16,
@@ -472,7 +475,8 @@ int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int h
     for (int S : cands) {
         if (S > n_max) break;
         const double t = model_time(S, batch, num_q_heads, num_kv_heads, head_dim, block_size,
-                                    n_max, nb.empty() ? nullptr : nb.data(), hpc, slots, ring);
+                                    n_max, nb.empty() ? nullptr : nb.data(), hpc, slots, ring,
+                                    kv8 ? 1.0 : 2.0);
         if (t < best_t * 0.995) {  // prefer fewer splits unless clearly faster
             best_t = t;
             best = S;
@@ -481,14 +485,32 @@ int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int h
     return best;
 }
 
+}  // namespace
+
+extern "C" {
+
+int kf_choose_num_splits_for(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_context_len,
+                             const int32_t *context_lens_host, int num_sms) {
+    return choose_splits(batch, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                         context_lens_host, num_sms, false);
+}
+
 int kf_choose_num_splits(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                          int block_size, int max_context_len, const int32_t *context_lens_host,
                          int device) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         return -1;
-    return kf_choose_num_splits_for(batch, num_q_heads, num_kv_heads, head_dim, block_size,
-                                    max_context_len, context_lens_host, sms);
+    return choose_splits(batch, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                         context_lens_host, sms, false);
+}
+
+int kf_choose_num_splits_fp8(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_context_len,
+                             const int32_t *context_lens_host, int num_sms) {
+    return choose_splits(batch, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                         context_lens_host, num_sms, true);
 }
 
 kf_status kf_merge_partials(const float *out_partial, const float *lse_partial,

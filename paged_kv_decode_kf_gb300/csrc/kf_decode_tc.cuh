@@ -562,7 +562,9 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
             }
 
             // S^T = K Q^T : rows = tokens, cols = query heads of the group
+            // two accumulators (even / odd k-steps) halve the dependent MMA chain
             float sc[4] = {0.f, 0.f, 0.f, 0.f};
+            float sd[4] = {0.f, 0.f, 0.f, 0.f};
             if (KV8) {
                 // one ldmatrix.x4 = 16 tokens x 32 d codes; each 32-bit register holds 4
                 // consecutive codes of one token, widened to the A fragment of k-step
@@ -578,7 +580,7 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
                         const uint32_t ra = fr[2 * h2], rb = fr[2 * h2 + 1];
                         const uint32_t af[4] = {e4m3x2_to_f16x2(ra), e4m3x2_to_f16x2(rb),
                                                 e4m3x2_to_f16x2(ra >> 16), e4m3x2_to_f16x2(rb >> 16)};
-                        mma_f16(sc, af, qb[2 * kk + h2][0], qb[2 * kk + h2][1]);
+                        mma_f16(h2 ? sd : sc, af, qb[2 * kk + h2][0], qb[2 * kk + h2][1]);
                     }
                 }
             } else {
@@ -589,9 +591,11 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
                     const uint32_t a = kbuf + (chunk >> 3) * Sh::kBoxBytes + swz<128>(t, chunk & 7);
                     uint32_t fr[4];
                     ldsm_x4(a, fr);
-                    mma_bf16(sc, fr, qb[ks][0], qb[ks][1]);
+                    mma_bf16((ks & 1) ? sd : sc, fr, qb[ks][0], qb[ks][1]);
                 }
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sc[e] += sd[e];
             // scores in base 2, masked past the end; sc[0..1] token g, sc[2..3] token g+8
             const float x0 = g < nvalid ? sc[0] * sl2 : -INFINITY;
             const float x1 = g < nvalid ? sc[1] * sl2 : -INFINITY;
@@ -807,11 +811,14 @@ cudaError_t launch_t(const DecodeParams &p, const StepParams &sp, cudaStream_t s
     return cudaGetLastError();
 }
 
-// Ring depth: about 96 KiB of loads in flight per CTA, 3 to 8 stages.
+// Ring depth: about 96 KiB of loads in flight per CTA for bf16 caches (two
+// CTAs per SM), 64 KiB for FP8 caches, whose per-stage instruction chain is
+// longer, so that three CTAs fit per SM; 3 to 8 stages.
 template <int D, int HPC, bool KV8>
 constexpr int stages_for() {
     constexpr int st = TcShape<D, HPC, 1, KV8>::kStageBytes;
-    return 98304 / st < 3 ? 3 : (98304 / st > 8 ? 8 : 98304 / st);
+    constexpr int ring = KV8 ? 65536 : 98304;
+    return ring / st < 3 ? 3 : (ring / st > 8 ? 8 : ring / st);
 }
 
 template <int D, int HPC, bool FUSED, bool KV8>

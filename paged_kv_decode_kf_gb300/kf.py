@@ -42,6 +42,8 @@ _lib.kf_choose_num_splits.restype = _i32
 _lib.kf_choose_num_splits.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _i32]
 _lib.kf_choose_num_splits_for.restype = _i32
 _lib.kf_choose_num_splits_for.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _i32]
+_lib.kf_choose_num_splits_fp8.restype = _i32
+_lib.kf_choose_num_splits_fp8.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _i32]
 _lib.kf_merge_partials.restype = _i32
 _lib.kf_merge_partials.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.kf_decode_step_workspace_size.restype = ctypes.c_size_t
@@ -124,14 +126,21 @@ def kf_append_kv(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor
 
 def kf_choose_num_splits(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                          block_size: int, max_context_len: int, context_lens_host=None,
-                         device: Optional[int] = None, num_sms: Optional[int] = None) -> int:
+                         device: Optional[int] = None, num_sms: Optional[int] = None,
+                         kv_dtype: str = "bf16") -> int:
     """The library's split count for this batch (host-side plan)."""
     arr = None
     ptr = None
     if context_lens_host is not None:
         arr = torch.as_tensor(context_lens_host, dtype=torch.int32).cpu().contiguous()
         ptr = arr.data_ptr()
-    if num_sms is not None:
+    if kv_dtype == "fp8":
+        if num_sms is None:
+            dev = torch.cuda.current_device() if device is None else device
+            num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        n = _lib.kf_choose_num_splits_fp8(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                          max_context_len, ptr, num_sms)
+    elif num_sms is not None:
         n = _lib.kf_choose_num_splits_for(batch, num_q_heads, num_kv_heads, head_dim, block_size,
                                           max_context_len, ptr, num_sms)
     else:

@@ -55,7 +55,8 @@ class DecodeStep:
     def plan(self, ctx_lens: torch.Tensor, max_ctx: int) -> int:
         w = self.w
         return kf.kf_choose_num_splits(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
-                                       w.block_size, max_ctx, ctx_lens.cpu().numpy().astype(np.int32))
+                                       w.block_size, max_ctx, ctx_lens.cpu().numpy().astype(np.int32),
+                                       kv_dtype=w.kv_dtype)
 
     @property
     def fp8(self) -> bool:
