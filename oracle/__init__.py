@@ -79,6 +79,11 @@ def _declare(lib) -> None:
     lib.kfo_append_fp8.restype = ctypes.c_int
     lib.kfo_append_fp8.argtypes = [_u8p, _u8p, _u16p, _u16p, _f32p, _f32p, _i32p, ctypes.c_int, _i32p,
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64]
+    lib.kfo_multiquery_partials.restype = ctypes.c_int
+    lib.kfo_multiquery_partials.argtypes = [
+        _u16p, _i32p, _u16p, _u16p, _i32p, ctypes.c_int, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_int,
+        ctypes.c_int64, _f64p, _f64p]
     lib.kfo_append.restype = ctypes.c_int
     lib.kfo_append.argtypes = [_u16p, _u16p, _u16p, _u16p, _i32p, ctypes.c_int, _i32p, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64]
@@ -288,4 +293,30 @@ def append_fp8(k_cache, v_cache, k_new, v_new, k_scale, v_scale, block_tables, c
         k2, v2, _u16(k_new), _u16(v_new), np.ascontiguousarray(k_scale, dtype=np.float32),
         np.ascontiguousarray(v_scale, dtype=np.float32), bt, bt.shape[1], ctx, bt.shape[0], hkv, d, bs, nb)
     return k2, v2, skipped
+
+
+# ----------------------------------------------------------------------------
+# Multi-query (chunked prefill / shared prefix) attention
+# ----------------------------------------------------------------------------
+
+def multiquery_partials(q, q_start, k_cache, v_cache, block_tables, ctx_lens, scale: float, causal: bool,
+                        num_splits: int = 1, max_context_len: Optional[int] = None,
+                        lib=None) -> Tuple[np.ndarray, np.ndarray]:
+    """Partials o [S, Nq, Hq, D], lse [S, Nq, Hq] of query tokens grouped by
+    request (q_start [B+1]) over each request's paged context."""
+    q, k_cache, v_cache = _u16(q), _u16(k_cache), _u16(v_cache)
+    qs, bt, ctx = _i32(q_start), _i32(block_tables), _i32(ctx_lens)
+    Nq, Hq, D = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    B = ctx.shape[0]
+    if max_context_len is None:
+        max_context_len = int(ctx.max()) if B else 0
+    o = np.full((num_splits, Nq, Hq, D), np.nan, dtype=np.float64)
+    lse = np.full((num_splits, Nq, Hq), np.nan, dtype=np.float64)
+    rc = (lib or load()).kfo_multiquery_partials(q, qs, k_cache, v_cache, bt, bt.shape[1], ctx, int(bool(causal)),
+                                                 B, Nq, Hq, hkv, D, bs, nb, scale, num_splits, max_context_len,
+                                                 o, lse)
+    if rc != 0:
+        raise ValueError("oracle multiquery_partials failed (rc=%d)" % rc)
+    return o, lse
 

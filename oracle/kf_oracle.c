@@ -36,6 +36,17 @@
  *    next position before attending (KernelFlume section 3.2, "Local
  *    attention on the attention nodes").
  *
+ *  - Multi-query (chunked prefill) attention: "Mathematical Formulation of
+ *    Chunked Attention" on the ultrainstinct.tech page -- the query chunk k of a
+ *    prompt attends to the keys of earlier chunks, held in the paged cache,
+ *    without a mask, and to its own chunk's keys with causal masking. With
+ *    the chunk already in the cache (L tokens in all, the chunk its last C),
+ *    query j (0-based in the chunk) sits at position L - C + j and attends to
+ *    tokens [0, L - C + j]. Non-causal: every query attends to all L tokens
+ *    (the shared-prefix pass of cascade attention, "What FlashInfer brings:
+ *    JIT and cascade attention" on blog.lo0.es: the prefix is attended once
+ *    for all requests, then merged with each request's own suffix).
+ *
  *  - FP8 KV cache: the decode posts on blog.lo0.es ("Quantised KV cache --
  *    --kv-cache-dtype fp8") store K/V in 8-bit floats with scales to halve the
  *    bytes decode reads. Here a cached element is an OCP FP8 E4M3 code c with
@@ -539,5 +550,61 @@ int kfo_append_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_new, co
         }
     }
     return skipped;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Multi-query (chunked prefill / shared prefix) attention                    */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Partials for query tokens grouped by request: request b owns query rows
+ * q_start[b] .. q_start[b+1]-1 (C_b of them) of q [num_q_tokens, Hq, D] and a
+ * context of L_b = ctx_lens[b] cached tokens (the chunk included). Query j of
+ * request b attends tokens [0, limit) with limit = L_b - C_b + j + 1 if causal,
+ * L_b otherwise; split s keeps the part of its token range (the decode split
+ * rule) below the limit. Writes o_part [S, num_q_tokens, Hq, D] and
+ * lse_part [S, num_q_tokens, Hq]. Returns -3 on C_b > L_b (causal) or a bad
+ * length, -1 on a bad block id.
+ */
+int kfo_multiquery_partials(const uint16_t *q, const int32_t *q_start, const uint16_t *k_cache,
+                            const uint16_t *v_cache, const int32_t *block_tables, int bt_stride,
+                            const int32_t *ctx_lens, int causal, int batch, int num_q_tokens,
+                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                            int64_t num_blocks, double scale, int num_splits,
+                            int64_t max_context_len, double *o_part, double *lse_part)
+{
+    if (num_splits < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0 || block_size < 1)
+        return -4;
+    int G = num_q_heads / num_kv_heads;
+    for (int b = 0; b < batch; ++b) {
+        int64_t L = ctx_lens[b];
+        int64_t C = (int64_t)q_start[b + 1] - q_start[b];
+        if (L < 0 || L > (int64_t)bt_stride * block_size || L > max_context_len || C < 0 ||
+            q_start[b + 1] > num_q_tokens || (causal && C > L))
+            return -3;
+        const int32_t *bt_row = block_tables + (int64_t)b * bt_stride;
+        for (int64_t j = 0; j < C; ++j) {
+            int64_t n = q_start[b] + j;
+            int64_t limit = causal ? L - C + j + 1 : L;
+            for (int h = 0; h < num_q_heads; ++h) {
+                const uint16_t *q_row = q + (n * num_q_heads + h) * head_dim;
+                for (int s = 0; s < num_splits; ++s) {
+                    int64_t t0, t1;
+                    kfo_split_range(L, block_size, num_splits, max_context_len, s, &t0, &t1);
+                    if (t1 > limit)
+                        t1 = limit;
+                    if (t0 > t1)
+                        t0 = t1;
+                    int64_t slot = ((int64_t)s * num_q_tokens + n) * num_q_heads + h;
+                    int rc = kfo_partial(q_row, k_cache, v_cache, bt_row, num_blocks, block_size,
+                                         num_kv_heads, head_dim, h / G, t0, t1, scale,
+                                         o_part + slot * head_dim, lse_part + slot);
+                    if (rc != 0)
+                        return rc;
+                }
+            }
+        }
+    }
+    return 0;
 }
 

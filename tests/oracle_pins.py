@@ -441,10 +441,86 @@ def pin_fp8_append(lib):
     assert np.array_equal(k2, ek) and np.array_equal(v2, ev)
 
 
+# ----------------------------------------------------------------------------
+# multi-query (chunked prefill / shared prefix) attention
+# ----------------------------------------------------------------------------
+
+def pin_golden_chunk(lib):
+    g = _load_golden()["chunk_causal"]
+    args = (_bf16(g["q"]), np.array(g["q_start"], np.int32), _bf16(g["k_cache"]), _bf16(g["v_cache"]),
+            np.array(g["block_tables"], np.int32), np.array(g["ctx_lens"], np.int32), g["scale"])
+    for causal, key in ((True, "causal"), (False, "full")):
+        o, l = oracle.multiquery_partials(*args, causal, lib=lib)
+        np.testing.assert_allclose(o[0], np.array(g["expect_%s_out" % key]), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l[0], np.array(g["expect_%s_lse" % key]), rtol=0, atol=1e-13)
+
+
+def _mq_case(lengths=(9, 30, 17), chunks=(3, 1, 5), hq=4, hkv=2, d=16, bs=4, seed=21):
+    w, inp = _small(batch=len(lengths), hq=hq, hkv=hkv, d=d, bs=bs, lengths=lengths, seed=seed)
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    rng = np.random.default_rng(seed)
+    q = _bf16(np.round(rng.standard_normal((int(q_start[-1]), hq, d)) * 8) / 8)
+    _, k, v, bt, ctx = _arrays(inp)
+    return w, q, q_start, k, v, bt, ctx
+
+
+def pin_multiquery_causal_rows(lib):
+    """Causal query j of a chunk of C equals plain attention over the first
+    L - C + j + 1 tokens; with C = 1 it is the decode partial itself."""
+    w, q, qs, k, v, bt, ctx = _mq_case()
+    o, l = oracle.multiquery_partials(q, qs, k, v, bt, ctx, w.scale, True, 3, max_context_len=32, lib=lib)
+    m_o, m_l = oracle.merge_partials(o, l, lib=lib)
+    for b in range(len(ctx)):
+        C = int(qs[b + 1] - qs[b])
+        for j in range(C):
+            n = int(qs[b]) + j
+            lim = np.array([int(ctx[b]) - C + j + 1], np.int32)
+            ref_o, ref_l = oracle.attention(q[n:n + 1], k, v, bt[b:b + 1], lim, w.scale, lib=lib)
+            np.testing.assert_allclose(m_o[n], ref_o[0], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(m_l[n], ref_l[0], rtol=1e-13, atol=1e-13)
+    # C = 1 for every request: the decode partials, split by split
+    qs1 = np.arange(len(ctx) + 1, dtype=np.int32)
+    q1 = q[:len(ctx)]
+    o1, l1 = oracle.multiquery_partials(q1, qs1, k, v, bt, ctx, w.scale, True, 3, max_context_len=32, lib=lib)
+    od, ld = oracle.decode_partials(q1, k, v, bt, ctx, w.scale, 3, max_context_len=32, lib=lib)
+    assert np.array_equal(o1, od) and np.array_equal(l1, ld)
+
+
+def pin_multiquery_noncausal_rows(lib):
+    w, q, qs, k, v, bt, ctx = _mq_case(seed=23)
+    o, l = oracle.multiquery_partials(q, qs, k, v, bt, ctx, w.scale, False, lib=lib)
+    for b in range(len(ctx)):
+        for n in range(int(qs[b]), int(qs[b + 1])):
+            ref_o, ref_l = oracle.attention(q[n:n + 1], k, v, bt[b:b + 1], ctx[b:b + 1], w.scale, lib=lib)
+            np.testing.assert_allclose(o[0, n], ref_o[0], rtol=0, atol=1e-12)
+
+
+def pin_cascade_merge(lib):
+    """Shared prefix attended once (non-causal, one table) merged with each
+    request's own suffix equals attention over prefix + suffix."""
+    bs, P = 4, 12                                 # prefix: 3 shared blocks
+    w, inp = _small(batch=3, hq=4, hkv=2, d=16, bs=bs, lengths=(P + 2, P + 7, P + 12), seed=29)
+    q, k, v, bt, ctx = _arrays(inp)
+    shared = bt[0, :P // bs].copy()
+    full_bt = bt.copy()
+    full_bt[:, :P // bs] = shared                 # every request's table starts with the shared blocks
+    o_full, l_full = oracle.attention(q, k, v, full_bt, ctx, w.scale, lib=lib)
+    qs = np.array([0, 3], np.int32)
+    o_p, l_p = oracle.multiquery_partials(q, qs, k, v, shared[None, :], np.array([P], np.int32), w.scale, False,
+                                          2, lib=lib)
+    suffix_bt = np.full_like(bt, -1)
+    suffix_bt[:, :bt.shape[1] - P // bs] = full_bt[:, P // bs:]
+    o_s, l_s = oracle.decode_partials(q, k, v, suffix_bt, ctx - P, w.scale, 2, lib=lib)
+    m_o, m_l = oracle.merge_partials(np.concatenate([o_p, o_s]), np.concatenate([l_p, l_s]), lib=lib)
+    np.testing.assert_allclose(m_o, o_full, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(m_l, l_full, rtol=1e-13, atol=1e-13)
+
+
 PINS = [
     pin_bf16_widening, pin_golden_two_token, pin_golden_gqa, pin_golden_merge, pin_golden_append,
     pin_context_len_one, pin_identical_keys, pin_scale_zero, pin_dominant_key, pin_head_mapping,
     pin_permutation_invariance, pin_split_ranges, pin_split_merge, pin_merge_properties,
     pin_shift_invariance, pin_scipy_brute_force, pin_append_random,
     pin_e4m3_decode, pin_e4m3_encode, pin_fp8_attention_is_dequantised_attention, pin_fp8_append,
+    pin_golden_chunk, pin_multiquery_causal_rows, pin_multiquery_noncausal_rows, pin_cascade_merge,
 ]

@@ -13,7 +13,7 @@ from oracle_pins import PINS
 SRC = os.path.join(os.path.dirname(oracle.__file__), "kf_oracle.c")
 
 MUTANTS = {
-    "interleaved_head_map": ("h / G, t0, t1", "h % j->hkv, t0, t1"),
+    "interleaved_head_map": ("h / G, t0, t1, j->scale", "h % j->hkv, t0, t1, j->scale"),
     "dropped_log_l": ("*lse = m + log(l);", "*lse = m;"),
     "dropped_max_in_lse": ("*lse = m + log(l);", "*lse = log(l);"),
     "missing_normalisation": ("        o[d] /= l;", "        o[d] /= 1.0;"),
@@ -38,6 +38,8 @@ MUTANTS = {
     "e4m3_overflow_to_nan": ("    if (a >= 448.0)\n        return sign | 0x7E;", "    if (a >= 448.0)\n        return sign | 0x7F;"),
     "fp8_v_scale_dropped": ("o[d] += p * (kfo_e4m3_to_double(v[d]) * v_scale);", "o[d] += p * kfo_e4m3_to_double(v[d]);"),
     "fp8_k_scale_is_v_scale": ("(double)k_scale[kvh],", "(double)v_scale[kvh],"),
+    "chunk_causal_off_by_one": ("int64_t limit = causal ? L - C + j + 1 : L;", "int64_t limit = causal ? L - C + j : L;"),
+    "chunk_causal_reversed": ("int64_t limit = causal ? L - C + j + 1 : L;", "int64_t limit = causal ? L - j : L;"),
     "fp8_append_multiplies": ("float kq = (float)kfo_bf16_to_double(k_new[src + d]) / k_scale[h];",
                               "float kq = (float)kfo_bf16_to_double(k_new[src + d]) * k_scale[h];"),
 }
