@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--decode-kernel", default="tc", choices=["tc", "simt"])
-    ap.add_argument("--path", default="auto", choices=["auto", "fused", "calls"],
+    ap.add_argument("--path", default="auto", choices=["auto", "fused", "calls", "cascade"],
                     help="fused: kf_decode_step (one launch); calls: append, attention, merge; "
                          "auto: fused for unsharded workloads with the tensor-core kernel")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
@@ -307,11 +307,19 @@ def run_ours(args):
     K = args.steps if args.steps is not None else default_steps(w.name)
     W = max(args.warmup, 3)
     dev = wl.make_inputs(w, "cuda:%d" % local)
-    fused = args.path == "fused" or (args.path == "auto" and not w.shards and args.decode_kernel == "tc")
+    fused = args.path == "fused" or (args.path == "auto" and not w.shards and not w.shared_prefix
+                                     and args.decode_kernel == "tc")
     if w.kv_dtype == "fp8" and args.decode_kernel != "tc":
         raise SystemExit("the FP8 cache is served by the tensor-core kernel only")
-    step = DecodeStep(dev, num_splits=args.num_splits, fused=fused)
-    kv_bytes = dev.kv_bytes()
+    cascade = bool(w.shared_prefix) and args.path in ("auto", "cascade")
+    if cascade:
+        from paged_kv_decode_kf_gb300.step import CascadeStep
+        step = CascadeStep(dev)
+        kv_bytes = step.unique_kv_bytes()      # the prefix once, each suffix once
+    else:
+        step = DecodeStep(dev, num_splits=args.num_splits, fused=fused)
+        kv_bytes = dev.kv_bytes()
+    logical_kv_bytes = dev.kv_bytes()          # sum over requests of their whole context
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -367,6 +375,9 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         names = ["q", "k_new", "v_new", "ctx_before", "ctx_after", "block_tables"]
+        for extra in ("prefix_table", "suffix_tables", "suffix_ctx_before", "suffix_ctx_after"):
+            if getattr(dev, extra) is not None:
+                names.append(extra)
         tensors = [getattr(dev, n) for n in names]
         if w.shards:
             names += ["tail_tables", "tail_ctx_before"]
@@ -394,7 +405,10 @@ def run_ours(args):
                 dev.shards[int(n[9:])].ctx_after = v
             else:
                 setattr(dev, n, v)
-        step_e = DecodeStep(dev, num_splits=step.num_splits, fused=step.fused)
+        if cascade:
+            step_e = CascadeStep(dev, prefix_splits=step.Sp, suffix_splits=step.Ss)
+        else:
+            step_e = DecodeStep(dev, num_splits=step.num_splits, fused=step.fused)
         ob = step_e.out.numel() * step_e.out.element_size()
         res_dev = torch.empty(ob + step_e.lse.numel() * 4, dtype=torch.uint8, device=dev.q.device)
         step_e.out = res_dev[:ob].view(step_e.out.dtype).view(step_e.out.shape)
@@ -428,6 +442,7 @@ def run_ours(args):
     per_launch_kv = kv_bytes / n_att
     traffic = profiled_traffic(w.name, "fused" if step.fused else args.decode_kernel, per_launch_kv)
     kname = ("decode step, one launch (append + attention + merge)" if step.fused
+             else "shared-prefix multi-query pass + suffix decode attention" if cascade
              else "decode attention (%s)" % args.decode_kernel)
     roofline = {"bound": "hbm", "achieved": att_gbs, "peak": peak, "unit": "GB/s", "frac": att_gbs / peak,
                 "traffic": traffic, "kernel": kname,
@@ -454,7 +469,11 @@ def run_ours(args):
                        "num_splits_source": "planner" if args.num_splits is None else "--num-splits",
                        "step": "append + split attention + LSE merge",
                        "path": "kf_decode_step (one launch)" if step.fused else
+                               ("kf_append_kv + kf_paged_multiquery_attention (prefix, once) + "
+                                "kf_paged_decode_attention (suffixes) + kf_merge_partials") if cascade else
                                "kf_append_kv + kf_paged_decode_attention x%d + kf_merge_partials" % n_att,
+                       "logical_kv_bytes_per_step": logical_kv_bytes,
+                       "effective_gbs": logical_kv_bytes / (ms * 1e-3) / 1e9,
                        "l2": "no flush: the %.2f GB of KV read per step exceeds the 129 MB L2" % (kv_bytes / 1e9)
                        if kv_bytes > L2_BYTES else "KV fits in L2 (launch-bound case)",
                        "parallelism": "replica per GPU" if world > 1 else "1 GPU"},

@@ -147,6 +147,49 @@ kf_status kf_paged_decode_attention(const void *q, const void *k_cache, const vo
                                     kf_stream_t stream);
 
 /*
+ * kf_paged_multiquery_attention -- paged attention of many query tokens per
+ * request: chunked prefill and speculative verify (causal = 1) and the
+ * shared-prefix pass of cascade attention (causal = 0).
+ *
+ * "Disaggregated Inference Architecture: Paged KV-Cache Tiering, Chunked
+ * Prefill, and Asynchronous Overlap" (ultrainstinct.tech), "Mathematical
+ * Formulation of Chunked Attention": a chunk's queries attend to earlier
+ * chunks' keys in the paged cache without a mask and to their own chunk
+ * causally. Request b owns query rows q_start[b] .. q_start[b+1]-1 (C_b of
+ * them) of q, and its cache holds L_b = context_lens[b] tokens with the chunk
+ * as the last C_b. Causal: query j (0-based in the chunk) attends tokens
+ * [0, L_b - C_b + j]; non-causal: all L_b tokens. Cascade attention ("What
+ * FlashInfer brings: JIT and cascade attention", blog.lo0.es) is one
+ * non-causal call with batch = 1, the prefix's table and q_start = {0, B}
+ * (every request's query), whose partials are merged by kf_merge_partials
+ * with those of kf_paged_decode_attention over each request's own suffix.
+ *
+ *   q             bf16 [num_q_tokens, num_q_heads, head_dim]
+ *   q_start       int32 [batch + 1] (device), ascending, q_start[batch] <= num_q_tokens
+ *   context_lens  int32 [batch]; causal calls need C_b <= L_b
+ *   max_context_len, max_query_len  host-side bounds of L_b and C_b
+ *   out_partial   f32 [num_splits, num_q_tokens, num_q_heads, head_dim]
+ *   lse_partial   f32 [num_splits, num_q_tokens, num_q_heads]
+ * Splits follow kf_paged_decode_attention's rule, each clipped to its query's
+ * limit; a (split, query) pair with no token gives (0, -inf). Rows of q not
+ * covered by q_start are not written. Merge with kf_merge_partials(batch =
+ * num_q_tokens). Accumulation fp32, inputs bf16.
+ * Host errors: null pointers, negative sizes, causal not 0/1 -> KF_ERR_INVALID;
+ * unsupported head_dim/block_size/group or batch * query tiles > 65535 ->
+ * KF_ERR_UNSUPPORTED. Device errors: KF_DEVERR_BLOCK_ID, KF_DEVERR_CONTEXT_LEN
+ * (length out of range, or C_b > L_b when causal), KF_DEVERR_MAX_CONTEXT
+ * (L_b above max_context_len or C_b above max_query_len).
+ */
+kf_status kf_paged_multiquery_attention(const void *q, const int32_t *q_start, const void *k_cache,
+                                        const void *v_cache, const int32_t *block_tables,
+                                        int bt_stride, const int32_t *context_lens, int causal,
+                                        int max_context_len, int max_query_len, int batch,
+                                        int num_q_tokens, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int64_t num_blocks,
+                                        float scale, int num_splits, float *out_partial,
+                                        float *lse_partial, kf_stream_t stream);
+
+/*
  * kf_choose_num_splits -- the split count the library would pick for a batch.
  *
  * A host-side plan (no device work): it models the decode kernel's schedule

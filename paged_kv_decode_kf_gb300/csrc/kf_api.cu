@@ -312,6 +312,63 @@ kf_status kf_paged_decode_attention_fp8(const void *q, const void *k_cache, cons
                           v_scale, true, stream);
 }
 
+kf_status kf_paged_multiquery_attention(const void *q, const int32_t *q_start, const void *k_cache,
+                                        const void *v_cache, const int32_t *block_tables,
+                                        int bt_stride, const int32_t *context_lens, int causal,
+                                        int max_context_len, int max_query_len, int batch,
+                                        int num_q_tokens, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int64_t num_blocks,
+                                        float scale, int num_splits, float *out_partial,
+                                        float *lse_partial, kf_stream_t stream) {
+    if (batch < 0 || num_q_tokens < 0 || num_splits < 1 || bt_stride < 1 || num_blocks < 1 ||
+        max_context_len < 0 || max_query_len < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
+        head_dim < 1 || block_size < 1 || !isfinite(scale) || (causal != 0 && causal != 1))
+        return KF_ERR_INVALID;
+    if (batch == 0 || num_q_tokens == 0) return KF_OK;
+    if (!q || !q_start || !k_cache || !v_cache || !block_tables || !context_lens || !out_partial ||
+        !lse_partial)
+        return KF_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out_partial))
+        return KF_ERR_INVALID;
+    if (head_dim != 128 && head_dim != 64) return KF_ERR_UNSUPPORTED;
+    if (!supported_dims(head_dim, block_size) || !supported_group(num_q_heads, num_kv_heads))
+        return KF_ERR_UNSUPPORTED;
+    if (num_splits > 65535) return KF_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return KF_ERR_CUDA;
+    MqParams p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.q_start = q_start;
+    p.k_cache = static_cast<const uint16_t *>(k_cache);
+    p.v_cache = static_cast<const uint16_t *>(v_cache);
+    p.block_tables = block_tables;
+    p.ctx_lens = context_lens;
+    p.out_partial = out_partial;
+    p.lse_partial = lse_partial;
+    p.err = dev->err;
+    p.num_blocks = num_blocks;
+    p.bt_stride = bt_stride;
+    p.max_context_len = max_context_len;
+    p.max_query_len = max_query_len;
+    p.batch = batch;
+    p.num_q_tokens = num_q_tokens;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    p.num_splits = num_splits;
+    const int64_t n_max = ((int64_t)max_context_len + block_size - 1) / block_size;
+    p.chunk_blocks = (int)std::max<int64_t>(1, (n_max + num_splits - 1) / num_splits);
+    p.causal = causal;
+    p.q_tiles = 1;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    void *fn = encode_fn();
+    if (!fn) return KF_ERR_CUDA;
+    const cudaError_t e = launch_multiquery(p, reinterpret_cast<cudaStream_t>(stream), fn);
+    if (e == cudaErrorInvalidValue) return KF_ERR_UNSUPPORTED;
+    return from_cuda(e);
+}
+
 size_t kf_decode_step_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                      int num_splits) {
     if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || num_splits < 1) return 0;

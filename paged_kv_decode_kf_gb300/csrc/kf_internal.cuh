@@ -48,6 +48,27 @@ struct StepArgs {
     int out_dtype;
 };
 
+// Parameters of one multi-query (chunked prefill / shared prefix) launch.
+struct MqParams {
+    const uint16_t *q;          // bf16 [num_q_tokens, Hq, D]
+    const int32_t *q_start;     // [batch + 1]
+    const uint16_t *k_cache;
+    const uint16_t *v_cache;
+    const int32_t *block_tables;
+    const int32_t *ctx_lens;    // [batch], tokens in the cache including the chunk
+    float *out_partial;         // f32 [S, num_q_tokens, Hq, D]
+    float *lse_partial;         // f32 [S, num_q_tokens, Hq]
+    unsigned int *err;
+    int64_t num_blocks;
+    int bt_stride;
+    int max_context_len, max_query_len;
+    int batch, num_q_tokens, num_q_heads, num_kv_heads, head_dim, block_size;
+    int num_splits, chunk_blocks, causal, q_tiles;
+    float scale_log2;
+};
+
+cudaError_t launch_multiquery(MqParams p, cudaStream_t stream, void *encode_fn);
+
 // Decode kernels, one per implementation. Each returns the launch status.
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream, void *encode_fn);

@@ -44,6 +44,9 @@ _lib.kf_choose_num_splits_for.restype = _i32
 _lib.kf_choose_num_splits_for.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _i32]
 _lib.kf_choose_num_splits_fp8.restype = _i32
 _lib.kf_choose_num_splits_fp8.argtypes = [_i32, _i32, _i32, _i32, _i32, _i32, _vp, _i32]
+_lib.kf_paged_multiquery_attention.restype = _i32
+_lib.kf_paged_multiquery_attention.argtypes = [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
+                                               _i32, _i32, _i32, _i32, _i64, _f32, _i32, _vp, _vp, _vp]
 _lib.kf_merge_partials.restype = _i32
 _lib.kf_merge_partials.argtypes = [_vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _vp, _vp]
 _lib.kf_decode_step_workspace_size.restype = ctypes.c_size_t
@@ -172,6 +175,32 @@ def kf_paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: t
         B, hq, hkv, d, bs, nb, float(scale), int(num_splits),
         _dev(out_partial, torch.float32, "out_partial"), _dev(lse_partial, torch.float32, "lse_partial"),
         _stream(stream)), "kf_paged_decode_attention")
+    return out_partial, lse_partial
+
+
+def kf_paged_multiquery_attention(q: torch.Tensor, q_start: torch.Tensor, k_cache: torch.Tensor,
+                                  v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                  causal: bool, max_context_len: int, max_query_len: int, scale: float,
+                                  num_splits: int, out_partial: Optional[torch.Tensor] = None,
+                                  lse_partial: Optional[torch.Tensor] = None,
+                                  stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Multi-query paged attention (chunked prefill / shared prefix); returns
+    (out_partial [S, Nq, Hq, D], lse_partial [S, Nq, Hq])."""
+    Nq, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    B = block_tables.shape[0]
+    if out_partial is None:
+        out_partial = torch.empty((num_splits, Nq, hq, d), dtype=torch.float32, device=q.device)
+    if lse_partial is None:
+        lse_partial = torch.empty((num_splits, Nq, hq), dtype=torch.float32, device=q.device)
+    _check(_lib.kf_paged_multiquery_attention(
+        _dev(q, torch.bfloat16, "q"), _dev(q_start, torch.int32, "q_start"),
+        _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
+        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, torch.int32, "context_lens"), int(bool(causal)), int(max_context_len),
+        int(max_query_len), B, Nq, hq, hkv, d, bs, nb, float(scale), int(num_splits),
+        _dev(out_partial, torch.float32, "out_partial"), _dev(lse_partial, torch.float32, "lse_partial"),
+        _stream(stream)), "kf_paged_multiquery_attention")
     return out_partial, lse_partial
 
 

@@ -113,3 +113,81 @@ class DecodeStep:
         if self.fused:
             return 1
         return int(self.with_append) + len(self.views) + 1
+
+
+class CascadeStep:
+    """A decode step for requests behind one shared prefix (cascade attention,
+    "What FlashInfer brings: JIT and cascade attention", blog.lo0.es): the
+    append goes through each request's suffix table; one non-causal
+    multi-query pass attends the prefix once for all B queries; decode
+    attention covers each request's suffix; one LSE merge combines the two
+    sets of partials."""
+
+    def __init__(self, inp: DecodeInputs, prefix_splits: Optional[int] = None,
+                 suffix_splits: Optional[int] = None, out_dtype=torch.float32):
+        w = inp.workload
+        assert w.shared_prefix and inp.prefix_table is not None
+        self.inp, self.w = inp, w
+        B, Hq = w.batch, w.num_q_heads
+        dev = inp.q.device
+        self.P = int(w.shared_prefix)
+        self.max_suffix = int(inp.suffix_ctx_after.max().item())
+        # prefix pass: KV heads x query tiles x splits CTAs; about 4 per SM
+        if prefix_splits is None:
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            units = w.num_kv_heads * max(1, -(-B * w.group // 64))
+            prefix_splits = max(1, min(self.P // w.block_size, -(-4 * sms // units)))
+        if suffix_splits is None:
+            suffix_splits = kf.kf_choose_num_splits(B, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                                    self.max_suffix,
+                                                    inp.suffix_ctx_after.cpu().numpy().astype(np.int32))
+        self.Sp, self.Ss = int(prefix_splits), int(suffix_splits)
+        self.q_start = torch.tensor([0, B], dtype=torch.int32, device=dev)
+        self.prefix_len = torch.tensor([self.P], dtype=torch.int32, device=dev)
+        S = self.Sp + self.Ss
+        self.out_partial = torch.empty((S, B, Hq, w.head_dim), dtype=torch.float32, device=dev)
+        self.lse_partial = torch.empty((S, B, Hq), dtype=torch.float32, device=dev)
+        self.out = torch.empty((B, Hq, w.head_dim), dtype=out_dtype, device=dev)
+        self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        self.fused = False
+        self.with_append = True
+
+    def append(self, stream=None) -> None:
+        i = self.inp
+        kf.kf_append_kv(i.k_new, i.v_new, i.k_cache, i.v_cache, i.suffix_tables, i.suffix_ctx_before, stream)
+
+    def attention(self, stream=None) -> None:
+        i, w, Sp = self.inp, self.w, self.Sp
+        kf.kf_paged_multiquery_attention(i.q, self.q_start, i.k_cache, i.v_cache, i.prefix_table, self.prefix_len,
+                                         False, self.P, w.batch, w.scale, Sp, self.out_partial[:Sp],
+                                         self.lse_partial[:Sp], stream)
+        kf.kf_paged_decode_attention(i.q, i.k_cache, i.v_cache, i.suffix_tables, i.suffix_ctx_after,
+                                     self.max_suffix, w.scale, self.Ss, self.out_partial[Sp:],
+                                     self.lse_partial[Sp:], stream)
+
+    def merge(self, stream=None) -> None:
+        kf.kf_merge_partials(self.out_partial, self.lse_partial, self.out, lse_out=self.lse, stream=stream)
+
+    def run(self, stream=None) -> None:
+        self.append(stream)
+        self.attention(stream)
+        self.merge(stream)
+
+    @property
+    def launches_per_step(self) -> int:
+        return 4
+
+    @property
+    def num_splits(self) -> int:
+        return self.Sp + self.Ss
+
+    @property
+    def views(self):
+        return [None, None]
+
+    def unique_kv_bytes(self) -> int:
+        """KV bytes the cascade step must read: the prefix once, each suffix once."""
+        w = self.w
+        tok = self.P + int(self.inp.suffix_ctx_after.to(torch.int64).sum().item())
+        return tok * w.kv_bytes_per_token()
+

@@ -117,6 +117,8 @@ class Workload:
     shards: int = 0                # >0: KV spread over this many token-range shards
     description: str = ""
     kv_dtype: str = "bf16"         # "bf16" or "fp8" (E4M3 codes with per-KV-head scales)
+    shared_prefix: int = 0         # >0: every request starts with these many shared tokens
+                                   # (whole blocks); `lengths` then draws the private suffixes
 
     @property
     def group(self) -> int:
@@ -160,6 +162,14 @@ CONFIGS = {
                     "179/64/13 requests from U[1K,8K]/U[8K,64K]/U[64K,128K]"),
 }
 
+# Shared-prefix batch for cascade attention (the pages' cascade example: many
+# requests behind one long common prompt), not one of the five configs.
+CONFIGS["cascade"] = Workload(
+    name="cascade", batch=64, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+    lengths=Uniform(64, 2048), seed=1005, shared_prefix=16384,
+    description="shared-prefix batch: 64 requests behind one 16K-token prefix, private suffixes "
+                "U[64,2048], 32/8 heads, D 128, bs 16")
+
 CONFIG_ORDER = ("tiny", "llama8b", "longctx", "shard4", "ragged")
 
 
@@ -175,7 +185,7 @@ def scaled(w: Workload, *, batch: Optional[int] = None, lengths=None, name=None,
         seed=seed if seed is not None else w.seed + 7919,
         spare_blocks=w.spare_blocks if spare_blocks is None else spare_blocks,
         num_splits=w.num_splits, shards=w.shards, description=w.description,
-        kv_dtype=kv_dtype or w.kv_dtype)
+        kv_dtype=kv_dtype or w.kv_dtype, shared_prefix=w.shared_prefix)
 
 
 def with_kv_dtype(w: Workload, kv_dtype: str) -> Workload:
@@ -184,7 +194,7 @@ def with_kv_dtype(w: Workload, kv_dtype: str) -> Workload:
                     head_dim=w.head_dim, block_size=w.block_size, lengths=w.lengths, seed=w.seed,
                     spare_blocks=w.spare_blocks, num_splits=w.num_splits, shards=w.shards,
                     description=w.description + ("" if kv_dtype == "bf16" else ", FP8 E4M3 KV cache"),
-                    kv_dtype=kv_dtype)
+                    kv_dtype=kv_dtype, shared_prefix=w.shared_prefix)
 
 
 def fp8_scales(num_kv_heads: int):
@@ -218,6 +228,11 @@ class DecodeInputs:
     # ... FP8 caches: k_cache/v_cache are uint8 E4M3 codes, with these scales
     k_scale: Optional[torch.Tensor] = field(default=None, kw_only=True)
     v_scale: Optional[torch.Tensor] = field(default=None, kw_only=True)
+    # ... shared-prefix batches: the prefix's table and each request's suffix
+    prefix_table: Optional[torch.Tensor] = field(default=None, kw_only=True)
+    suffix_tables: Optional[torch.Tensor] = field(default=None, kw_only=True)
+    suffix_ctx_before: Optional[torch.Tensor] = field(default=None, kw_only=True)
+    suffix_ctx_after: Optional[torch.Tensor] = field(default=None, kw_only=True)
     ctx_before: torch.Tensor
     ctx_after: torch.Tensor
     num_blocks: int
@@ -245,7 +260,9 @@ class DecodeInputs:
             ctx_before=mv(self.ctx_before), ctx_after=mv(self.ctx_after), num_blocks=self.num_blocks,
             shards=[ShardView(mv(s.block_tables), mv(s.ctx_after), s.first_block) for s in self.shards],
             tail_tables=mv(self.tail_tables), tail_ctx_before=mv(self.tail_ctx_before),
-            k_scale=mv(self.k_scale), v_scale=mv(self.v_scale))
+            k_scale=mv(self.k_scale), v_scale=mv(self.v_scale), prefix_table=mv(self.prefix_table),
+            suffix_tables=mv(self.suffix_tables), suffix_ctx_before=mv(self.suffix_ctx_before),
+            suffix_ctx_after=mv(self.suffix_ctx_after))
 
 
 def _bf16_normal(shape, gen: torch.Generator, device) -> torch.Tensor:
@@ -267,6 +284,9 @@ class Layout:
     shard_first_block: list = field(default_factory=list)  # int64 [B] per shard
     tail_tables: Optional[np.ndarray] = None
     tail_ctx_before: Optional[np.ndarray] = None
+    prefix_table: Optional[np.ndarray] = None       # int32 [1, prefix blocks]
+    suffix_tables: Optional[np.ndarray] = None      # int32 [B, max suffix blocks]
+    suffix_ctx_before: Optional[np.ndarray] = None  # int64 [B]
 
 
 def plan_layout(w: Workload, lengths: Optional[Sequence[int]] = None) -> Layout:
@@ -279,6 +299,8 @@ def plan_layout(w: Workload, lengths: Optional[Sequence[int]] = None) -> Layout:
     else:
         L0 = np.asarray(lengths, dtype=np.int64)
         assert L0.shape == (B,)
+    if w.shared_prefix:
+        return _plan_shared_prefix(w, L0, rng)
     L1 = L0 + 1
     n_blocks = (L1 + bs - 1) // bs
     max_blocks = int(n_blocks.max()) if B else 1
@@ -294,6 +316,32 @@ def plan_layout(w: Workload, lengths: Optional[Sequence[int]] = None) -> Layout:
     if w.shards > 0:
         _plan_shards(lay, w.shards, bs)
     return lay
+
+
+def _plan_shared_prefix(w: Workload, suffix0: np.ndarray, rng) -> Layout:
+    """Every request's table starts with the same prefix blocks (the first
+    physical ids drawn), followed by its own suffix blocks."""
+    B, bs, P = w.batch, w.block_size, w.shared_prefix
+    assert P % bs == 0, "the shared prefix must be whole blocks"
+    NP = P // bs
+    L0 = suffix0 + P
+    L1 = L0 + 1
+    n_suffix = (suffix0 + 1 + bs - 1) // bs
+    NB = NP + int(n_suffix.sum()) + w.spare_blocks
+    perm = rng.permutation(NB)
+    prefix = perm[:NP].astype(np.int32)
+    n_blocks = NP + n_suffix
+    bt = np.full((B, int(n_blocks.max())), -1, dtype=np.int32)
+    st = np.full((B, max(int(n_suffix.max()), 1)), -1, dtype=np.int32)
+    pos = NP
+    for b in range(B):
+        ns = int(n_suffix[b])
+        bt[b, :NP] = prefix
+        bt[b, NP:NP + ns] = perm[pos:pos + ns]
+        st[b, :ns] = perm[pos:pos + ns]
+        pos += ns
+    return Layout(ctx_before=L0, ctx_after=L1, n_blocks=n_blocks, block_tables=bt, num_blocks=NB,
+                  prefix_table=prefix[None, :].copy(), suffix_tables=st, suffix_ctx_before=suffix0)
 
 
 def _plan_shards(lay: Layout, n_shards: int, bs: int) -> None:
@@ -360,6 +408,11 @@ def make_inputs(w: Workload, device="cpu", lengths: Optional[Sequence[int]] = No
     if lay.tail_tables is not None:
         inp.tail_tables = i32(lay.tail_tables)
         inp.tail_ctx_before = i32(lay.tail_ctx_before)
+    if lay.prefix_table is not None:
+        inp.prefix_table = i32(lay.prefix_table)
+        inp.suffix_tables = i32(lay.suffix_tables)
+        inp.suffix_ctx_before = i32(lay.suffix_ctx_before)
+        inp.suffix_ctx_after = i32(lay.suffix_ctx_before + 1)
     return inp
 
 

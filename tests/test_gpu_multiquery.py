@@ -1,0 +1,105 @@
+"""GPU parity of multi-query paged attention (chunked prefill / speculative
+verify, causal; shared-prefix pass of cascade attention, non-causal)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import check_lse, check_out, check_partials
+from paged_kv_decode_kf_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kf():
+    import __graft_entry__ as g
+    g.build()
+    from paged_kv_decode_kf_gb300 import kf
+    assert kf.kf_get_device_error() == 0
+    return kf
+
+
+@pytest.fixture(autouse=True)
+def no_device_error(kf):
+    yield
+    assert kf.kf_get_device_error() == 0, "a kernel raised a device error"
+
+
+def _case(lengths, chunks, hq=32, hkv=8, d=128, bs=16, seed=5):
+    """Contexts of L_b tokens (chunk included) with C_b query tokens each."""
+    w = wl.Workload(name="mq", batch=len(lengths), num_q_heads=hq, num_kv_heads=hkv, head_dim=d, block_size=bs,
+                    lengths=wl.Fixed(tuple(L - 1 for L in lengths)), seed=seed, spare_blocks=2)
+    dev = wl.make_inputs(w, "cuda")
+    q_start = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed + 1)
+    q = torch.randn((int(q_start[-1]), hq, d), generator=gen, device="cuda", dtype=torch.bfloat16)
+    return w, dev, q, torch.tensor(q_start, device="cuda")
+
+
+def _host(dev, q, qs):
+    return (wl.bf16_bits(q), qs.cpu().numpy(), wl.bf16_bits(dev.k_cache), wl.bf16_bits(dev.v_cache),
+            dev.block_tables.cpu().numpy(), dev.ctx_after.cpu().numpy())
+
+
+CASES = {
+    "spec_verify": ((300, 1000, 77, 4096), (4, 4, 4, 4)),
+    "mixed_chunks": ((9, 30, 17, 100, 64), (3, 1, 5, 32, 64)),
+    "long_chunk": ((2048, 700), (128, 700)),
+}
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("S", [1, 3])
+def test_multiquery(kf, name, causal, S):
+    lengths, chunks = CASES[name]
+    w, dev, q, qs = _case(lengths, chunks)
+    hq_, qs_h, k, v, bt, ctx = _host(dev, q, qs)
+    maxL, maxC = int(max(lengths)), int(max(chunks))
+    o_p, l_p = kf.kf_paged_multiquery_attention(q, qs, dev.k_cache, dev.v_cache, dev.block_tables, dev.ctx_after,
+                                                causal, maxL, maxC, w.scale, S)
+    out, lse = kf.kf_merge_partials(o_p, l_p)
+    ref_po, ref_pl = oracle.multiquery_partials(hq_, qs_h, k, v, bt, ctx, w.scale, causal, S, max_context_len=maxL)
+    check_partials(o_p.cpu().numpy(), l_p.cpu().numpy(), ref_po, ref_pl, name + " partials")
+    ref_o, ref_l = oracle.merge_partials(ref_po, ref_pl)
+    check_out(out.cpu().numpy(), ref_o, name + " out")
+    check_lse(lse.cpu().numpy(), ref_l, name + " lse")
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2), (16, 2), (8, 1)])
+@pytest.mark.parametrize("d,bs", [(64, 16), (128, 32)])
+def test_multiquery_shapes(kf, hq, hkv, d, bs):
+    w, dev, q, qs = _case((40, 97, 33), (7, 2, 33), hq=hq, hkv=hkv, d=d, bs=bs, seed=hq + hkv + d)
+    hq_, qs_h, k, v, bt, ctx = _host(dev, q, qs)
+    o_p, l_p = kf.kf_paged_multiquery_attention(q, qs, dev.k_cache, dev.v_cache, dev.block_tables, dev.ctx_after,
+                                                True, 97, 33, w.scale, 2)
+    ref_po, ref_pl = oracle.multiquery_partials(hq_, qs_h, k, v, bt, ctx, w.scale, True, 2, max_context_len=97)
+    check_partials(o_p.cpu().numpy(), l_p.cpu().numpy(), ref_po, ref_pl, "mq shapes")
+
+
+def test_cascade_prefix_plus_suffix(kf):
+    """Prefix attended once for all requests, merged with each suffix, equals
+    decode attention over each request's full table."""
+    from paged_kv_decode_kf_gb300.step import CascadeStep
+    w = wl.scaled(wl.CONFIGS["cascade"], batch=6, lengths=wl.Fixed((5, 70, 300, 1, 16, 999)))
+    dev = wl.make_inputs(w, "cuda")
+    hv_k, hv_v = wl.bf16_bits(dev.k_cache), wl.bf16_bits(dev.v_cache)
+    step = CascadeStep(dev)
+    step.run()
+    torch.cuda.synchronize()
+    k2, v2, _ = oracle.append(hv_k, hv_v, wl.bf16_bits(dev.k_new), wl.bf16_bits(dev.v_new),
+                              dev.block_tables.cpu().numpy(), dev.ctx_before.cpu().numpy())
+    ref_o, ref_l = oracle.attention(wl.bf16_bits(dev.q), k2, v2, dev.block_tables.cpu().numpy(),
+                                    dev.ctx_after.cpu().numpy(), w.scale)
+    check_out(step.out.cpu().numpy(), ref_o, "cascade out")
+    check_lse(step.lse.cpu().numpy(), ref_l, "cascade lse")
+
+
+def test_multiquery_rejects_bad_q_start(kf):
+    w, dev, q, qs = _case((40, 50), (3, 3))
+    bad = torch.tensor([0, 3, 99], dtype=torch.int32, device="cuda")   # past num_q_tokens
+    kf.kf_paged_multiquery_attention(q, bad, dev.k_cache, dev.v_cache, dev.block_tables, dev.ctx_after,
+                                     True, 50, 3, w.scale, 1)
+    assert kf.kf_get_device_error() & kf.KF_DEVERR_CONTEXT_LEN
