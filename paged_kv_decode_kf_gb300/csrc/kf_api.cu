@@ -161,6 +161,17 @@ int decode_impl() {
     return (s && strcmp(s, "simt") == 0) ? 1 : 0;
 }
 
+// Multi-query kernel choice: the tcgen05 kernel's 128-row tile pays off once a
+// request brings at least 64 (query, head) rows per KV head; below that the
+// mma.sync kernel's 32/64-column tiles waste less. KF_MQ_IMPL = "mma" or
+// "tc05" forces one (read per call, so a process can compare them).
+bool multiquery_on_tc05(int max_query_len, int group) {
+    const char *s = getenv("KF_MQ_IMPL");
+    if (s && strcmp(s, "mma") == 0) return false;
+    if (s && strcmp(s, "tc05") == 0) return true;
+    return (int64_t)max_query_len * group >= 64;
+}
+
 }  // namespace kf
 
 using namespace kf;
@@ -364,7 +375,9 @@ kf_status kf_paged_multiquery_attention(const void *q, const int32_t *q_start, c
     p.scale_log2 = scale * 1.4426950408889634f;
     void *fn = encode_fn();
     if (!fn) return KF_ERR_CUDA;
-    const cudaError_t e = launch_multiquery(p, reinterpret_cast<cudaStream_t>(stream), fn);
+    const cudaError_t e = multiquery_on_tc05(max_query_len, num_q_heads / num_kv_heads)
+                              ? launch_multiquery_tc05(p, reinterpret_cast<cudaStream_t>(stream), fn)
+                              : launch_multiquery(p, reinterpret_cast<cudaStream_t>(stream), fn);
     if (e == cudaErrorInvalidValue) return KF_ERR_UNSUPPORTED;
     return from_cuda(e);
 }

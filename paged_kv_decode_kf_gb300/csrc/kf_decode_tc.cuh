@@ -123,6 +123,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            int c3, int c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -410,16 +419,34 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
     bool ok = true;
     if (warp == HPC) {
         // ------------------------------ producer ------------------------------
-        if (lane == 0) {
-            for (int i = 0; i < n_sub; ++i) {
-                const int st = i % NS;
-                if (!mbar_wait(bars + 8 * (NS + st), ((i / NS) & 1) ^ 1)) {
-                    raise_error(p.err, KF_DEVERR_TIMEOUT);
-                    break;
+        // The whole warp walks the stages: table entries come 32 at a time (one
+        // coalesced load, lane e holds logical block base + e), so a TMA issue
+        // never waits on a dependent load; lane 0 waits for slots and issues.
+        const int bs_shift = block_shift(p.block_size);
+        int64_t tab_base = -1;
+        int32_t tab_ent = -1;
+        for (int i = 0; i < n_sub; ++i) {
+            const int st = i % NS;
+            int go = 1;
+            if (lane == 0 && !mbar_wait(bars + 8 * (NS + st), ((i / NS) & 1) ^ 1)) {
+                raise_error(p.err, KF_DEVERR_TIMEOUT);
+                go = 0;
+            }
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
+            const int64_t t_base = (sb0 + i) * kTok;
+            const int64_t lb = t_base >> bs_shift;
+            if (tab_base < 0 || lb >= tab_base + 32) {
+                tab_base = lb;
+                const int64_t e = lb + lane;
+                tab_ent = e < p.bt_stride ? p.block_tables[(int64_t)b * p.bt_stride + e] : -1;
+            }
+            int64_t phys = __shfl_sync(0xffffffffu, tab_ent, (int)(lb - tab_base));
+            if (lane == 0) {
+                if (phys < 0 || phys >= p.num_blocks) {
+                    raise_error(p.err, KF_DEVERR_BLOCK_ID);
+                    phys = 0;
                 }
-                const int64_t t_base = (sb0 + i) * kTok;
-                const int64_t phys = physical_block(p, b, t_base / p.block_size);
-                const int slot = (int)(t_base % p.block_size);
+                const int slot = (int)(t_base & (p.block_size - 1));
                 const uint32_t full = bars + 8 * st;
                 const uint32_t dst = base + st * Sh::kStageBytes;
                 mbar_arrive_expect_tx(full, Sh::kStageBytes);

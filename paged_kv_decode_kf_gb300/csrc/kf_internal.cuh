@@ -68,6 +68,8 @@ struct MqParams {
 };
 
 cudaError_t launch_multiquery(MqParams p, cudaStream_t stream, void *encode_fn);
+// tcgen05 version (128-row query tiles, TMEM accumulators); same contract.
+cudaError_t launch_multiquery_tc05(MqParams p, cudaStream_t stream, void *encode_fn);
 
 // Decode kernels, one per implementation. Each returns the launch status.
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);
@@ -139,6 +141,10 @@ __device__ __forceinline__ SplitRange split_range(const DecodeParams &p, int b, 
 
 // Physical block of logical block `lb` of request b, redirected to block 0
 // (and reported) if the table entry is out of range.
+// log2 of a power-of-two block size (every supported size is one): hot loops
+// shift and mask instead of dividing a 64-bit token index.
+__device__ __forceinline__ int block_shift(int block_size) { return 31 - __clz(block_size); }
+
 __device__ __forceinline__ int64_t physical_block(const DecodeParams &p, int b, int64_t lb) {
     int64_t phys = p.block_tables[(int64_t)b * p.bt_stride + lb];
     if (phys < 0 || phys >= p.num_blocks) {

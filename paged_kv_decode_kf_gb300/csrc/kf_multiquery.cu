@@ -121,20 +121,32 @@ mq_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
 
     if (warp == NW) {
         // ------------------------------ producer ------------------------------
-        if (lane == 0) {
-            for (int i = 0; i < n_sub; ++i) {
-                const int st = i % NS;
-                if (!mbar_wait(bars + 8 * (NS + st), ((i / NS) & 1) ^ 1)) {
-                    raise_error(p.err, KF_DEVERR_TIMEOUT);
-                    break;
-                }
-                const int64_t t_base = (sb0 + i) * kTok;
-                int64_t phys = p.block_tables[(int64_t)b * p.bt_stride + t_base / p.block_size];
+        // whole warp: table entries 32 at a time, lane 0 waits and issues
+        const int bs_shift = block_shift(p.block_size);
+        int64_t tab_base = -1;
+        int32_t tab_ent = -1;
+        for (int i = 0; i < n_sub; ++i) {
+            const int st = i % NS;
+            int go = 1;
+            if (lane == 0 && !mbar_wait(bars + 8 * (NS + st), ((i / NS) & 1) ^ 1)) {
+                raise_error(p.err, KF_DEVERR_TIMEOUT);
+                go = 0;
+            }
+            if (!__shfl_sync(0xffffffffu, go, 0)) break;
+            const int64_t t_base = (sb0 + i) * kTok;
+            const int64_t lb = t_base >> bs_shift;
+            if (tab_base < 0 || lb >= tab_base + 32) {
+                tab_base = lb;
+                const int64_t e = lb + lane;
+                tab_ent = e < p.bt_stride ? p.block_tables[(int64_t)b * p.bt_stride + e] : -1;
+            }
+            int64_t phys = __shfl_sync(0xffffffffu, tab_ent, (int)(lb - tab_base));
+            if (lane == 0) {
                 if (phys < 0 || phys >= p.num_blocks) {
                     raise_error(p.err, KF_DEVERR_BLOCK_ID);
                     phys = 0;
                 }
-                const int slot = (int)(t_base % p.block_size);
+                const int slot = (int)(t_base & (p.block_size - 1));
                 const uint32_t full = bars + 8 * st;
                 const uint32_t dst = base + st * Sh::kStageBytes;
                 mbar_arrive_expect_tx(full, Sh::kStageBytes);

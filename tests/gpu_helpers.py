@@ -21,17 +21,30 @@ LSE_REL = 1e-4
 
 
 @contextmanager
-def decode_impl(name: str):
-    """Select the decode kernel ("tc" or "simt") for the calls in the block."""
-    old = os.environ.get("KF_DECODE_IMPL")
-    os.environ["KF_DECODE_IMPL"] = name
+def _env(var: str, value: str):
+    old = os.environ.get(var)
+    os.environ[var] = value
     try:
         yield
     finally:
         if old is None:
-            os.environ.pop("KF_DECODE_IMPL", None)
+            os.environ.pop(var, None)
         else:
-            os.environ["KF_DECODE_IMPL"] = old
+            os.environ[var] = old
+
+
+def decode_impl(name: str):
+    """Select the decode kernel ("tc" or "simt") for the calls in the block."""
+    return _env("KF_DECODE_IMPL", name)
+
+
+@contextmanager
+def mq_impl(name: str):
+    """Select the multi-query kernel for the calls in the block: "mma", "tc05"
+    (one 128-row query tile per CTA), "tc05x2" (two tiles per CTA) or "auto"."""
+    with _env("KF_MQ_IMPL", "tc05" if name.startswith("tc05") else name), \
+            _env("KF_MQ_TILES", "2" if name == "tc05x2" else "1"):
+        yield
 
 
 class HostView:

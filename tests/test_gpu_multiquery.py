@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import check_lse, check_out, check_partials
+from gpu_helpers import HostView, check_lse, check_out, check_partials, mq_impl
 from paged_kv_decode_kf_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -50,16 +50,21 @@ CASES = {
 }
 
 
+IMPLS = ["mma", "tc05", "tc05x2"]
+
+
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("name", sorted(CASES))
 @pytest.mark.parametrize("S", [1, 3])
-def test_multiquery(kf, name, causal, S):
+def test_multiquery(kf, name, causal, S, impl):
     lengths, chunks = CASES[name]
     w, dev, q, qs = _case(lengths, chunks)
     hq_, qs_h, k, v, bt, ctx = _host(dev, q, qs)
     maxL, maxC = int(max(lengths)), int(max(chunks))
-    o_p, l_p = kf.kf_paged_multiquery_attention(q, qs, dev.k_cache, dev.v_cache, dev.block_tables, dev.ctx_after,
-                                                causal, maxL, maxC, w.scale, S)
+    with mq_impl(impl):
+        o_p, l_p = kf.kf_paged_multiquery_attention(q, qs, dev.k_cache, dev.v_cache, dev.block_tables,
+                                                    dev.ctx_after, causal, maxL, maxC, w.scale, S)
     out, lse = kf.kf_merge_partials(o_p, l_p)
     ref_po, ref_pl = oracle.multiquery_partials(hq_, qs_h, k, v, bt, ctx, w.scale, causal, S, max_context_len=maxL)
     check_partials(o_p.cpu().numpy(), l_p.cpu().numpy(), ref_po, ref_pl, name + " partials")
@@ -68,18 +73,21 @@ def test_multiquery(kf, name, causal, S):
     check_lse(lse.cpu().numpy(), ref_l, name + " lse")
 
 
+@pytest.mark.parametrize("impl", IMPLS)
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 2), (16, 2), (8, 1)])
 @pytest.mark.parametrize("d,bs", [(64, 16), (128, 32)])
-def test_multiquery_shapes(kf, hq, hkv, d, bs):
+def test_multiquery_shapes(kf, hq, hkv, d, bs, impl):
     w, dev, q, qs = _case((40, 97, 33), (7, 2, 33), hq=hq, hkv=hkv, d=d, bs=bs, seed=hq + hkv + d)
     hq_, qs_h, k, v, bt, ctx = _host(dev, q, qs)
-    o_p, l_p = kf.kf_paged_multiquery_attention(q, qs, dev.k_cache, dev.v_cache, dev.block_tables, dev.ctx_after,
-                                                True, 97, 33, w.scale, 2)
+    with mq_impl(impl):
+        o_p, l_p = kf.kf_paged_multiquery_attention(q, qs, dev.k_cache, dev.v_cache, dev.block_tables,
+                                                    dev.ctx_after, True, 97, 33, w.scale, 2)
     ref_po, ref_pl = oracle.multiquery_partials(hq_, qs_h, k, v, bt, ctx, w.scale, True, 2, max_context_len=97)
     check_partials(o_p.cpu().numpy(), l_p.cpu().numpy(), ref_po, ref_pl, "mq shapes")
 
 
-def test_cascade_prefix_plus_suffix(kf):
+@pytest.mark.parametrize("impl", IMPLS)
+def test_cascade_prefix_plus_suffix(kf, impl):
     """Prefix attended once for all requests, merged with each suffix, equals
     decode attention over each request's full table."""
     from paged_kv_decode_kf_gb300.step import CascadeStep
@@ -87,7 +95,8 @@ def test_cascade_prefix_plus_suffix(kf):
     dev = wl.make_inputs(w, "cuda")
     hv_k, hv_v = wl.bf16_bits(dev.k_cache), wl.bf16_bits(dev.v_cache)
     step = CascadeStep(dev)
-    step.run()
+    with mq_impl(impl):
+        step.run()
     torch.cuda.synchronize()
     k2, v2, _ = oracle.append(hv_k, hv_v, wl.bf16_bits(dev.k_new), wl.bf16_bits(dev.v_new),
                               dev.block_tables.cpu().numpy(), dev.ctx_before.cpu().numpy())
@@ -97,9 +106,30 @@ def test_cascade_prefix_plus_suffix(kf):
     check_lse(step.lse.cpu().numpy(), ref_l, "cascade lse")
 
 
-def test_multiquery_rejects_bad_q_start(kf):
+@pytest.mark.parametrize("impl", IMPLS)
+def test_multiquery_rejects_bad_q_start(kf, impl):
     w, dev, q, qs = _case((40, 50), (3, 3))
     bad = torch.tensor([0, 3, 99], dtype=torch.int32, device="cuda")   # past num_q_tokens
-    kf.kf_paged_multiquery_attention(q, bad, dev.k_cache, dev.v_cache, dev.block_tables, dev.ctx_after,
-                                     True, 50, 3, w.scale, 1)
+    with mq_impl(impl):
+        kf.kf_paged_multiquery_attention(q, bad, dev.k_cache, dev.v_cache, dev.block_tables, dev.ctx_after,
+                                         True, 50, 3, w.scale, 1)
     assert kf.kf_get_device_error() & kf.KF_DEVERR_CONTEXT_LEN
+
+
+def test_cascade_full_size_sampled(kf):
+    """The cascade workload at full size (64 requests behind a 16384-token
+    shared prefix, 4 query heads per KV head: 256 rows per KV head, the
+    tcgen05 kernel's shape) in the launch configuration the benchmark times;
+    sampled requests against the oracle over their whole tables."""
+    from paged_kv_decode_kf_gb300.step import CascadeStep
+    w = wl.CONFIGS["cascade"]
+    dev = wl.make_inputs(w, "cuda")
+    reqs = [0, 1, 31, 62, 63]
+    hv = HostView(dev, reqs)
+    step = CascadeStep(dev)
+    step.run()
+    torch.cuda.synchronize()
+    k2, v2 = hv.appended()
+    ref_o, ref_l = oracle.attention(hv.q, k2, v2, hv.tables[0], hv.ctx_after, w.scale)
+    check_out(step.out.float().cpu().numpy()[reqs], ref_o, "cascade full out")
+    check_lse(step.lse.cpu().numpy()[reqs], ref_l, "cascade full lse")
