@@ -161,15 +161,19 @@ int decode_impl() {
     return (s && strcmp(s, "simt") == 0) ? 1 : 0;
 }
 
-// Multi-query kernel choice: the tcgen05 kernel's 128-row tile pays off once a
-// request brings at least 64 (query, head) rows per KV head; below that the
-// mma.sync kernel's 32/64-column tiles waste less. KF_MQ_IMPL = "mma" or
-// "tc05" forces one (read per call, so a process can compare them).
-bool multiquery_on_tc05(int max_query_len, int group) {
+// Multi-query kernel choice: 0 = mma.sync (32/64-column tiles), 1 = tcgen05
+// with one 128-row query tile and 64-token KV tiles, 2 = tcgen05 with two
+// query tiles and 128-token KV tiles. The 128-row tile pays off from 64 (query,
+// head) rows per KV head; two tiles once a request has more than 128.
+// KF_MQ_IMPL = "mma", "tc05" or "tc05w" forces one (read per call, so a process
+// can compare them; "tc05w" needs more than 128 rows).
+int multiquery_kernel(int max_query_len, int group) {
+    const int64_t rows = (int64_t)max_query_len * group;
     const char *s = getenv("KF_MQ_IMPL");
-    if (s && strcmp(s, "mma") == 0) return false;
-    if (s && strcmp(s, "tc05") == 0) return true;
-    return (int64_t)max_query_len * group >= 64;
+    if (s && strcmp(s, "mma") == 0) return 0;
+    if (s && strcmp(s, "tc05") == 0) return 1;
+    if (s && strcmp(s, "tc05w") == 0) return rows > 128 ? 2 : 1;
+    return rows > 128 ? 2 : (rows >= 64 ? 1 : 0);
 }
 
 }  // namespace kf
@@ -375,9 +379,11 @@ kf_status kf_paged_multiquery_attention(const void *q, const int32_t *q_start, c
     p.scale_log2 = scale * 1.4426950408889634f;
     void *fn = encode_fn();
     if (!fn) return KF_ERR_CUDA;
-    const cudaError_t e = multiquery_on_tc05(max_query_len, num_q_heads / num_kv_heads)
-                              ? launch_multiquery_tc05(p, reinterpret_cast<cudaStream_t>(stream), fn)
-                              : launch_multiquery(p, reinterpret_cast<cudaStream_t>(stream), fn);
+    const int which = multiquery_kernel(max_query_len, num_q_heads / num_kv_heads);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = which == 2   ? launch_multiquery_tc05w(p, st, fn)
+                          : which == 1 ? launch_multiquery_tc05(p, st, fn)
+                                       : launch_multiquery(p, st, fn);
     if (e == cudaErrorInvalidValue) return KF_ERR_UNSUPPORTED;
     return from_cuda(e);
 }

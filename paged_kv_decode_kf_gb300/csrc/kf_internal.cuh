@@ -70,6 +70,8 @@ struct MqParams {
 cudaError_t launch_multiquery(MqParams p, cudaStream_t stream, void *encode_fn);
 // tcgen05 version (128-row query tiles, TMEM accumulators); same contract.
 cudaError_t launch_multiquery_tc05(MqParams p, cudaStream_t stream, void *encode_fn);
+// tcgen05, 128-token KV tiles and two query tiles per CTA (> 128 rows per KV head).
+cudaError_t launch_multiquery_tc05w(MqParams p, cudaStream_t stream, void *encode_fn);
 
 // Decode kernels, one per implementation. Each returns the launch status.
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);

@@ -52,13 +52,13 @@
 // Precision: scores and O accumulate in fp32; P enters the PV product as
 // bf16 (relative error <= 2^-9 per weight, unbiased rounding), l sums the
 // unrounded fp32 weights.
-#include "kf_decode_tc.cuh"
-#include "kf_tc05.cuh"
+#include "kf_mq_tc05.cuh"
 
 namespace kf {
 namespace {
 
 using namespace tc;
+using namespace mq5;
 
 constexpr int kRows = 128;  // query rows per tile: M of both products
 constexpr int kTile = 64;   // tokens per KV tile
@@ -89,43 +89,6 @@ struct T5Shape {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
-// Packed two-lane fp32 operations (f32x2 forms of sm_100 and later), the
-// three-input max and the hardware base-2 exponential (flushes subnormal
-// results to zero; exp2(-inf) = 0).
-__device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
-__device__ __forceinline__ float ex2f(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// All lanes of the warp see the same outcome of a bounded wait.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity));
-}
 
 template <int D, int G, int QT>
 __global__ void __launch_bounds__(T5Shape<D, QT>::kThreads, QT == 1 ? 2 : 1)
@@ -545,19 +508,6 @@ cudaError_t launch_t5_g(const MqParams &p, cudaStream_t stream, const CUtensorMa
         case 8: return launch_t5<D, 8, QT>(p, stream, mk, mv);
     }
     return cudaErrorInvalidValue;
-}
-
-bool encode_block_map(tc::EncodeFn fn, CUtensorMap *map, const void *cache, const MqParams &p) {
-    const int halves = p.head_dim / 64;
-    const cuuint64_t row = (cuuint64_t)p.num_kv_heads * p.head_dim * 2;  // bytes between slots
-    const cuuint64_t dims[5] = {64, 8, (cuuint64_t)p.num_kv_heads * halves, (cuuint64_t)p.block_size / 8,
-                                (cuuint64_t)p.num_blocks};
-    const cuuint64_t strides[4] = {row, 128, 8 * row, row * p.block_size};
-    const cuuint32_t box[5] = {64, 8, (cuuint32_t)halves, (cuuint32_t)p.block_size / 8, 1};
-    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace

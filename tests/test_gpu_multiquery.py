@@ -50,7 +50,7 @@ CASES = {
 }
 
 
-IMPLS = ["mma", "tc05", "tc05x2"]
+IMPLS = ["mma", "tc05", "tc05x2", "tc05w"]
 
 
 @pytest.mark.parametrize("impl", IMPLS)
