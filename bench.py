@@ -345,6 +345,8 @@ def run_ours(args):
     # ---- device-timed region ----
     n_att = len(step.views)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    # cascade: append | prefix pass | suffix decode | merge, each bracketed
+    evc = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)] if cascade else None
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
@@ -358,6 +360,18 @@ def run_ours(args):
             step.step_fused()
             ev[i][1].record(stream)
             continue
+        if cascade:
+            e = evc[i]
+            e[0].record(stream)
+            step.append()
+            e[1].record(stream)
+            step.prefix()
+            e[2].record(stream)
+            step.suffix()
+            e[3].record(stream)
+            step.merge()
+            e[4].record(stream)
+            continue
         if step.with_append:
             step.append()
         ev[i][0].record(stream)
@@ -370,7 +384,11 @@ def run_ours(args):
     t1 = time.time()
     clk = clocks.stop(t0, t1)
     ms = start.elapsed_time(end) / K
-    att_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    if cascade:
+        phase_ms = [sum(e[k].elapsed_time(e[k + 1]) for e in evc) / K for k in range(4)]
+        att_ms = phase_ms[1] + phase_ms[2]
+    else:
+        att_ms = sum(a.elapsed_time(b) for a, b in ev) / K
     from paged_kv_decode_kf_gb300 import kf
     flags = kf.kf_get_device_error()
     if flags:
@@ -452,17 +470,30 @@ def run_ours(args):
     peak, peak_src = hbm_peak()
     att_gbs = kv_bytes / (att_ms * 1e-3) / 1e9
     if cascade:
-        # the shared-prefix pass is a dense contraction (every query against every
-        # prefix key): report against the bf16 tensor roofline. Algorithmic FLOPs
-        # = 4 * Hq * D * (sum of all requests' context lengths).
-        flops = 4.0 * w.num_q_heads * w.head_dim * float(dev.ctx_after.to(torch.int64).sum().item())
+        # Two kernels carry the step: the shared-prefix pass, a dense contraction
+        # (every query against every prefix key: 4 D FLOPs per token and query
+        # row) bound by the bf16 tensor pipe, and the suffix decode, bound by
+        # HBM. The roofline reports the one that takes longer; both are in
+        # "kernels".
         tpk, tsrc = tensor_peak()
-        achieved_tf = flops / (att_ms * 1e-3) / 1e12
-        roofline_override = {"bound": "tensor", "achieved": achieved_tf, "peak": tpk, "unit": "TFLOP/s",
-                             "frac": achieved_tf / tpk, "traffic": None,
-                             "algorithmic_flops_per_step": flops, "peak_source": tsrc,
-                             "kernel": "shared-prefix multi-query pass + suffix decode attention",
-                             "hbm_achieved_gbs": att_gbs, "hbm_frac": att_gbs / peak}
+        pre_s, suf_s = phase_ms[1] * 1e-3, phase_ms[2] * 1e-3
+        pre_tf = step.prefix_flops() / pre_s / 1e12
+        suf_gbs = step.suffix_kv_bytes() / suf_s / 1e9
+        kernels = {"append_us": phase_ms[0] * 1e3, "prefix_pass_us": phase_ms[1] * 1e3,
+                   "suffix_decode_us": phase_ms[2] * 1e3, "merge_us": phase_ms[3] * 1e3,
+                   "prefix_pass": {"bound": "tensor", "achieved": pre_tf, "peak": tpk, "unit": "TFLOP/s",
+                                   "frac": pre_tf / tpk, "algorithmic_flops": step.prefix_flops(),
+                                   "peak_source": tsrc},
+                   "suffix_decode": {"bound": "hbm", "achieved": suf_gbs, "peak": peak, "unit": "GB/s",
+                                     "frac": suf_gbs / peak, "algorithmic_bytes": step.suffix_kv_bytes()}}
+        dom = kernels["prefix_pass"] if pre_s >= suf_s else kernels["suffix_decode"]
+        roofline_override = dict(dom, traffic=None,
+                                 kernel="shared-prefix multi-query pass" if pre_s >= suf_s
+                                 else "suffix decode attention",
+                                 peak_source=(lambda src: src + (", of measured" if src.startswith("measured")
+                                                                 else ", of fallback"))(
+                                     tsrc if pre_s >= suf_s else peak_src),
+                                 kernels=kernels)
     else:
         roofline_override = None
     per_launch_kv = kv_bytes / n_att

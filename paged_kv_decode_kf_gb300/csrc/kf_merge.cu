@@ -10,11 +10,13 @@
 // KernelFlume (academ.us/article/2606.29207) section 5.1: merging the
 // partials of a partition of the tokens equals attention over all of them.
 //
-// Mapping: one CTA per (b, h) row; P groups of D/4 threads each take every
-// P-th partial (so S partials are read P at a time, coalesced 16-byte vectors,
-// 4 loads in flight per thread), then the groups' sums are combined in shared
-// memory. The row max M is found first by all threads striding over the S
-// lse values.
+// Mapping: one warp per (b, h) row, 8 rows per CTA, no block-level
+// synchronisation. Lane k loads lse of partials k, k + 32, ...; a shuffle
+// reduction gives M; each lane turns its lse into a weight, and the weights of
+// 32 partials at a time are broadcast by shuffles while the lanes load the
+// non-empty partials' o rows (16-byte vectors at D = 128, 8 at D = 64), eight
+// partials in flight. An empty partial (lse = -inf) has weight 0 and its o is
+// not read.
 #include <math.h>
 
 #include "kf_internal.cuh"
@@ -22,76 +24,91 @@
 namespace kf {
 namespace {
 
-constexpr int kGroups = 8;  // partial groups per row
+constexpr int kRowsPerCta = 8;
+constexpr int kInFlight = 8;  // partials loaded together
 
 template <int D>
-__global__ void __launch_bounds__(kGroups *(D / 4))
+struct MergeVec;
+template <>
+struct MergeVec<128> {
+    using T = float4;
+    static __device__ __forceinline__ void fma(float w, const T &o, T &a) {
+        a.x = fmaf(w, o.x, a.x); a.y = fmaf(w, o.y, a.y); a.z = fmaf(w, o.z, a.z); a.w = fmaf(w, o.w, a.w);
+    }
+    static __device__ __forceinline__ T zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+};
+template <>
+struct MergeVec<64> {
+    using T = float2;
+    static __device__ __forceinline__ void fma(float w, const T &o, T &a) {
+        a.x = fmaf(w, o.x, a.x); a.y = fmaf(w, o.y, a.y);
+    }
+    static __device__ __forceinline__ T zero() { return make_float2(0.f, 0.f); }
+};
+
+template <int D>
+__global__ void __launch_bounds__(32 * kRowsPerCta)
 merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part, int S,
              int64_t rows, void *__restrict__ out, int out_dtype, float *__restrict__ lse_out) {
-    constexpr int TPR = D / 4;  // threads per group: 4 outputs each
-    const int64_t row = blockIdx.x;
-    const int c = threadIdx.x % TPR, grp = threadIdx.x / TPR;
-
-    __shared__ float sm_red[kGroups * TPR / 32 + 1];
-    __shared__ __align__(16) float4 sm_acc[kGroups][TPR];
-    __shared__ float sm_w[kGroups];
+    using MV = MergeVec<D>;
+    using T = typename MV::T;
+    constexpr int V = D / 32;  // floats per lane
+    const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
 
     // 1. M = max_s lse_s
     float M = -INFINITY;
-    for (int s = threadIdx.x; s < S; s += blockDim.x) M = fmaxf(M, lse_part[(int64_t)s * rows + row]);
+    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldg(lse_part + (int64_t)s * rows + row));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if ((threadIdx.x & 31) == 0) sm_red[threadIdx.x >> 5] = M;
-    __syncthreads();
-    M = -INFINITY;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) M = fmaxf(M, sm_red[i]);
 
-    // 2. this group's share of sum_s w_s o_s and sum_s w_s
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    // 2. sum_s w_s o_s and sum_s w_s, w_s = e^{lse_s - M}
+    T acc = MV::zero();
     float wsum = 0.f;
     if (M != -INFINITY) {
-#pragma unroll 4
-        for (int s = grp; s < S; s += kGroups) {
-            const float l = lse_part[(int64_t)s * rows + row];
-            if (l == -INFINITY) continue;  // empty partial: weight 0, o not read
-            const float w = expf(l - M);
-            const float4 o = reinterpret_cast<const float4 *>(o_part + ((int64_t)s * rows + row) * D)[c];
-            acc.x = fmaf(w, o.x, acc.x);
-            acc.y = fmaf(w, o.y, acc.y);
-            acc.z = fmaf(w, o.z, acc.z);
-            acc.w = fmaf(w, o.w, acc.w);
+        for (int c0 = 0; c0 < S; c0 += 32) {
+            const int sl = c0 + lane;
+            const float l = sl < S ? __ldg(lse_part + (int64_t)sl * rows + row) : -INFINITY;
+            const float w = l == -INFINITY ? 0.f : expf(l - M);
             wsum += w;
+            const int n = S - c0 < 32 ? S - c0 : 32;
+            for (int u0 = 0; u0 < n; u0 += kInFlight) {
+                T o[kInFlight];
+                float wu[kInFlight];
+#pragma unroll
+                for (int u = 0; u < kInFlight; ++u) {
+                    wu[u] = __shfl_sync(0xffffffffu, w, (u0 + u) & 31);
+                    if (u0 + u >= n) wu[u] = 0.f;
+                    o[u] = wu[u] != 0.f
+                               ? __ldg(reinterpret_cast<const T *>(o_part + ((int64_t)(c0 + u0 + u) * rows + row) * D) + lane)
+                               : MV::zero();
+                }
+#pragma unroll
+                for (int u = 0; u < kInFlight; ++u) MV::fma(wu[u], o[u], acc);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+        const float inv = 1.f / wsum;
+        float *a = reinterpret_cast<float *>(&acc);
+#pragma unroll
+        for (int i = 0; i < V; ++i) a[i] *= inv;
+    }
+
+    // 3. write
+    const float *a = reinterpret_cast<const float *>(&acc);
+    if (out_dtype == KF_F32) {
+        reinterpret_cast<T *>(static_cast<float *>(out) + row * D)[lane] = acc;
+    } else {
+        uint16_t *o16 = static_cast<uint16_t *>(out) + row * D + V * lane;
+#pragma unroll
+        for (int i = 0; i < V; i += 2) {
+            __nv_bfloat162 v = __floats2bfloat162_rn(a[i], a[i + 1]);
+            *reinterpret_cast<__nv_bfloat162 *>(o16 + i) = v;
         }
     }
-    sm_acc[grp][c] = acc;
-    if (c == 0) sm_w[grp] = wsum;
-    __syncthreads();
-    if (grp != 0) return;
-
-    // 3. combine the groups and write
-    wsum = 0.f;
-    acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int g = 0; g < kGroups; ++g) {
-        const float4 a = sm_acc[g][c];
-        acc.x += a.x; acc.y += a.y; acc.z += a.z; acc.w += a.w;
-        wsum += sm_w[g];
-    }
-    if (M != -INFINITY) {
-        const float inv = 1.f / wsum;
-        acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-    }
-    if (out_dtype == KF_F32) {
-        reinterpret_cast<float4 *>(static_cast<float *>(out) + row * D)[c] = acc;
-    } else {
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-        uint2 v;
-        v.x = *reinterpret_cast<uint32_t *>(&lo);
-        v.y = *reinterpret_cast<uint32_t *>(&hi);
-        reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + row * D)[c] = v;
-    }
-    if (lse_out != nullptr && c == 0) lse_out[row] = (M == -INFINITY) ? -INFINITY : M + logf(wsum);
+    if (lse_out != nullptr && lane == 0) lse_out[row] = (M == -INFINITY) ? -INFINITY : M + logf(wsum);
 }
 
 }  // namespace
@@ -101,13 +118,14 @@ cudaError_t launch_merge(const float *out_partial, const float *lse_partial, int
                          float *lse_out, cudaStream_t stream) {
     const int64_t rows = (int64_t)batch * num_q_heads;
     if (rows == 0) return cudaSuccess;
-    if (rows > 0x7fffffff) return cudaErrorInvalidValue;
+    const int64_t ctas = (rows + kRowsPerCta - 1) / kRowsPerCta;
+    if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
     if (head_dim == 128)
-        merge_kernel<128><<<(unsigned)rows, kGroups * 32, 0, stream>>>(
-            out_partial, lse_partial, num_partials, rows, out, out_dtype, lse_out);
+        merge_kernel<128><<<(unsigned)ctas, 32 * kRowsPerCta, 0, stream>>>(out_partial, lse_partial, num_partials,
+                                                                         rows, out, out_dtype, lse_out);
     else
-        merge_kernel<64><<<(unsigned)rows, kGroups * 16, 0, stream>>>(
-            out_partial, lse_partial, num_partials, rows, out, out_dtype, lse_out);
+        merge_kernel<64><<<(unsigned)ctas, 32 * kRowsPerCta, 0, stream>>>(out_partial, lse_partial, num_partials,
+                                                                        rows, out, out_dtype, lse_out);
     return cudaGetLastError();
 }
 

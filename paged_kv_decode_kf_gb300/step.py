@@ -132,11 +132,16 @@ class CascadeStep:
         dev = inp.q.device
         self.P = int(w.shared_prefix)
         self.max_suffix = int(inp.suffix_ctx_after.max().item())
-        # prefix pass: KV heads x query tiles x splits CTAs; about 4 per SM
+        # prefix pass: one wave of CTAs (KV heads x query tiles x splits) for the
+        # kernel the library picks for B x G rows per KV head: 256 rows and one
+        # CTA per SM (tcgen05, two tiles), 128 rows and two per SM (tcgen05, one
+        # tile), 64 columns and about four per SM (mma.sync)
         if prefix_splits is None:
             sms = torch.cuda.get_device_properties(dev).multi_processor_count
-            units = w.num_kv_heads * max(1, -(-B * w.group // 64))
-            prefix_splits = max(1, min(self.P // w.block_size, -(-4 * sms // units)))
+            rows = B * w.group
+            rows_per_cta, per_sm = (256, 1) if rows > 128 else ((128, 2) if rows >= 64 else (64, 4))
+            units = w.num_kv_heads * max(1, -(-rows // rows_per_cta))
+            prefix_splits = max(1, min(self.P // w.block_size, -(-per_sm * sms // units)))
         if suffix_splits is None:
             suffix_splits = kf.kf_choose_num_splits(B, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
                                                     self.max_suffix,
@@ -156,14 +161,23 @@ class CascadeStep:
         i = self.inp
         kf.kf_append_kv(i.k_new, i.v_new, i.k_cache, i.v_cache, i.suffix_tables, i.suffix_ctx_before, stream)
 
-    def attention(self, stream=None) -> None:
+    def prefix(self, stream=None) -> None:
+        """The shared prefix, attended once by every request's query."""
         i, w, Sp = self.inp, self.w, self.Sp
         kf.kf_paged_multiquery_attention(i.q, self.q_start, i.k_cache, i.v_cache, i.prefix_table, self.prefix_len,
                                          False, self.P, w.batch, w.scale, Sp, self.out_partial[:Sp],
                                          self.lse_partial[:Sp], stream)
+
+    def suffix(self, stream=None) -> None:
+        """Each request's own blocks after the prefix."""
+        i, w, Sp = self.inp, self.w, self.Sp
         kf.kf_paged_decode_attention(i.q, i.k_cache, i.v_cache, i.suffix_tables, i.suffix_ctx_after,
                                      self.max_suffix, w.scale, self.Ss, self.out_partial[Sp:],
                                      self.lse_partial[Sp:], stream)
+
+    def attention(self, stream=None) -> None:
+        self.prefix(stream)
+        self.suffix(stream)
 
     def merge(self, stream=None) -> None:
         kf.kf_merge_partials(self.out_partial, self.lse_partial, self.out, lse_out=self.lse, stream=stream)
@@ -184,6 +198,14 @@ class CascadeStep:
     @property
     def views(self):
         return [None, None]
+
+    def prefix_flops(self) -> float:
+        """Algorithmic FLOPs of the prefix pass: 4 D per (token, query row)."""
+        w = self.w
+        return 4.0 * w.head_dim * w.num_q_heads * w.batch * self.P
+
+    def suffix_kv_bytes(self) -> int:
+        return int(self.inp.suffix_ctx_after.to(torch.int64).sum().item()) * self.w.kv_bytes_per_token()
 
     def unique_kv_bytes(self) -> int:
         """KV bytes the cascade step must read: the prefix once, each suffix once."""
