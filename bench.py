@@ -44,9 +44,12 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b")
     ap.add_argument("--decode-kernel", default="tc", choices=["tc", "simt"])
-    ap.add_argument("--path", default="auto", choices=["auto", "fused", "calls", "cascade"],
+    ap.add_argument("--path", default="auto", choices=["auto", "fused", "calls", "cascade", "cascade-calls"],
                     help="fused: kf_decode_step (one launch); calls: append, attention, merge; "
-                         "auto: fused for unsharded workloads with the tensor-core kernel")
+                         "cascade (shared-prefix workloads): prefix pass + kf_decode_step_merge_partials; "
+                         "cascade-calls: append, prefix pass, suffix decode, merge; "
+                         "auto: fused for unsharded workloads with the tensor-core kernel, cascade with a "
+                         "shared prefix")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="cache element type (fp8 = E4M3 codes with per-KV-head scales)")
     ap.add_argument("--num-splits", type=int, default=None,
@@ -323,10 +326,10 @@ def run_ours(args):
                                      and args.decode_kernel == "tc")
     if w.kv_dtype == "fp8" and args.decode_kernel != "tc":
         raise SystemExit("the FP8 cache is served by the tensor-core kernel only")
-    cascade = bool(w.shared_prefix) and args.path in ("auto", "cascade")
+    cascade = bool(w.shared_prefix) and args.path in ("auto", "cascade", "cascade-calls")
     if cascade:
         from paged_kv_decode_kf_gb300.step import CascadeStep
-        step = CascadeStep(dev)
+        step = CascadeStep(dev, fused_suffix=args.path != "cascade-calls")
         kv_bytes = step.unique_kv_bytes()      # the prefix once, each suffix once
     else:
         step = DecodeStep(dev, num_splits=args.num_splits, fused=fused)
@@ -362,6 +365,13 @@ def run_ours(args):
             continue
         if cascade:
             e = evc[i]
+            if step.fused_suffix:   # prefix pass | suffix step (append + attention + merge)
+                e[0].record(stream)
+                step.prefix()
+                e[1].record(stream)
+                step.suffix_step()
+                e[2].record(stream)
+                continue
             e[0].record(stream)
             step.append()
             e[1].record(stream)
@@ -385,7 +395,10 @@ def run_ours(args):
     clk = clocks.stop(t0, t1)
     ms = start.elapsed_time(end) / K
     if cascade:
-        phase_ms = [sum(e[k].elapsed_time(e[k + 1]) for e in evc) / K for k in range(4)]
+        nph = 2 if step.fused_suffix else 4
+        phase_ms = [sum(e[k].elapsed_time(e[k + 1]) for e in evc) / K for k in range(nph)]
+        if step.fused_suffix:   # as (append, prefix, suffix, merge) with the fused ones inside "suffix"
+            phase_ms = [0.0, phase_ms[0], phase_ms[1], 0.0]
         att_ms = phase_ms[1] + phase_ms[2]
     else:
         att_ms = sum(a.elapsed_time(b) for a, b in ev) / K
@@ -436,7 +449,7 @@ def run_ours(args):
             else:
                 setattr(dev, n, v)
         if cascade:
-            step_e = CascadeStep(dev, prefix_splits=step.Sp, suffix_splits=step.Ss)
+            step_e = CascadeStep(dev, prefix_splits=step.Sp, suffix_splits=step.Ss, fused_suffix=step.fused_suffix)
         else:
             step_e = DecodeStep(dev, num_splits=step.num_splits, fused=step.fused)
         ob = step_e.out.numel() * step_e.out.element_size()
@@ -479,7 +492,10 @@ def run_ours(args):
         pre_s, suf_s = phase_ms[1] * 1e-3, phase_ms[2] * 1e-3
         pre_tf = step.prefix_flops() / pre_s / 1e12
         suf_gbs = step.suffix_kv_bytes() / suf_s / 1e9
-        kernels = {"append_us": phase_ms[0] * 1e3, "prefix_pass_us": phase_ms[1] * 1e3,
+        kernels = {"path": "2 launches: prefix pass, then kf_decode_step_merge_partials (append + suffix "
+                           "attention + merge with the prefix partials)" if step.fused_suffix else
+                           "4 launches: append, prefix pass, suffix decode, merge",
+                   "append_us": phase_ms[0] * 1e3, "prefix_pass_us": phase_ms[1] * 1e3,
                    "suffix_decode_us": phase_ms[2] * 1e3, "merge_us": phase_ms[3] * 1e3,
                    "prefix_pass": {"bound": "tensor", "achieved": pre_tf, "peak": tpk, "unit": "TFLOP/s",
                                    "frac": pre_tf / tpk, "algorithmic_flops": step.prefix_flops(),
@@ -528,7 +544,9 @@ def run_ours(args):
                        "num_splits_source": "planner" if args.num_splits is None else "--num-splits",
                        "step": "append + split attention + LSE merge",
                        "path": "kf_decode_step (one launch)" if step.fused else
-                               ("kf_append_kv + kf_paged_multiquery_attention (prefix, once) + "
+                               ("kf_paged_multiquery_attention (prefix, once) + kf_decode_step_merge_partials "
+                                "(append + suffixes + merge)" if step.fused_suffix else
+                                "kf_append_kv + kf_paged_multiquery_attention (prefix, once) + "
                                 "kf_paged_decode_attention (suffixes) + kf_merge_partials") if cascade else
                                "kf_append_kv + kf_paged_decode_attention x%d + kf_merge_partials" % n_att,
                        "logical_kv_bytes_per_step": logical_kv_bytes,

@@ -289,6 +289,41 @@ kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, vo
                          kf_stream_t stream);
 
 /*
+ * kf_decode_step_merge_partials -- kf_decode_step whose final LSE merge also
+ * takes num_extra partials computed elsewhere: the one-launch form of the
+ * suffix step of cascade attention ("What FlashInfer brings: JIT and cascade
+ * attention", blog.lo0.es), where the extra partials are those of the shared
+ * prefix (kf_paged_multiquery_attention, causal = 0, batch = 1) and the
+ * block tables are each request's own blocks after the prefix. The merge is
+ * the exact one of kf_merge_partials ("Mathematical Formulation of Chunked
+ * Attention", ultrainstinct.tech; KernelFlume section 5.1) over this step's
+ * non-empty splits and the extra slots together, so the result equals
+ * attention over the tokens of both.
+ *
+ *   extra_out_partial  f32 [num_extra, batch, num_q_heads, head_dim], 16-byte aligned
+ *   extra_lse_partial  f32 [num_extra, batch, num_q_heads]; -inf marks an empty
+ *                      slot (its o is not read)
+ *   num_extra          >= 0; 0 is kf_decode_step
+ *   workspace          as kf_decode_step, and required whenever num_extra > 0
+ *                      (the merge counts its work units there even at num_splits = 1)
+ * Everything else, and the error behaviour, as kf_decode_step, plus:
+ * num_extra < 0, or num_extra > 0 with a null or misaligned extra pointer ->
+ * KF_ERR_INVALID; num_splits + num_extra too large for the merge to fit in
+ * the kernel's shared memory -> KF_ERR_UNSUPPORTED. The extra partials must be
+ * complete when the call runs (e.g. written earlier on the same stream).
+ */
+kf_status kf_decode_step_merge_partials(const void *q, const void *k_new, const void *v_new,
+                                        void *k_cache, void *v_cache, const int32_t *block_tables,
+                                        int bt_stride, const int32_t *context_lens_before,
+                                        int max_context_len, int batch, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int64_t num_blocks, float scale, int num_splits,
+                                        const float *extra_out_partial,
+                                        const float *extra_lse_partial, int num_extra,
+                                        void *workspace, size_t workspace_bytes, void *out,
+                                        kf_dtype out_dtype, float *lse_out, kf_stream_t stream);
+
+/*
  * FP8 (E4M3) KV cache: kf_append_kv_fp8, kf_paged_decode_attention_fp8,
  * kf_decode_step_fp8.
  *

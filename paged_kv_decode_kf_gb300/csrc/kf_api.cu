@@ -407,14 +407,16 @@ kf_status step_impl(const void *q, const void *k_new, const void *v_new, void *k
                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                     int64_t num_blocks, float scale, int num_splits, void *workspace,
                     size_t workspace_bytes, void *out, kf_dtype out_dtype, float *lse_out,
-                    const float *k_scale, const float *v_scale, bool kv8, kf_stream_t stream) {
+                    const float *k_scale, const float *v_scale, bool kv8, const float *ex_o,
+                    const float *ex_lse, int n_ex, kf_stream_t stream) {
     if (batch < 0 || num_splits < 1 || bt_stride < 1 || num_blocks < 1 || max_context_len < 0 ||
         num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || !isfinite(scale) ||
-        (out_dtype != KF_BF16 && out_dtype != KF_F32))
+        (out_dtype != KF_BF16 && out_dtype != KF_F32) || n_ex < 0)
         return KF_ERR_INVALID;
     if (batch == 0) return KF_OK;
     if (!q || !k_new || !v_new || !k_cache || !v_cache || !block_tables || !context_lens_before ||
-        !out || (kv8 && (!k_scale || !v_scale)))
+        !out || (kv8 && (!k_scale || !v_scale)) ||
+        (n_ex > 0 && (!ex_o || !ex_lse || !aligned16(ex_o))))
         return KF_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) ||
         !aligned16(v_cache) || !aligned16(out))
@@ -424,13 +426,14 @@ kf_status step_impl(const void *q, const void *k_new, const void *v_new, void *k
     if (batch > 65535 || num_splits > 65535) return KF_ERR_UNSUPPORTED;
     const size_t need = kf_decode_step_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
                                                       num_splits);
-    if (num_splits > 1 && (!workspace || !aligned16(workspace) || workspace_bytes < need))
+    const bool counted = num_splits > 1 || n_ex > 0;  // some group merges: counters needed
+    if (counted && (!workspace || !aligned16(workspace) || workspace_bytes < need))
         return KF_ERR_INVALID;
     // the last CTA of a group merges in its shared-memory ring: S x rows x 4 bytes must fit
     int hpc = 1, cps = 1;
     decode_tc_shape(num_kv_heads, head_dim, block_size, kv8, &hpc, &cps);
     const int R = hpc * (num_q_heads / num_kv_heads);
-    if ((int64_t)num_splits * R * 4 + 8 * R > decode_tc_ring_bytes(num_kv_heads, head_dim, kv8))
+    if (((int64_t)num_splits + n_ex) * R * 4 + 8 * R > decode_tc_ring_bytes(num_kv_heads, head_dim, kv8))
         return KF_ERR_UNSUPPORTED;
     DeviceInfo *dev = nullptr;
     if (device_info(&dev) != cudaSuccess) return KF_ERR_CUDA;
@@ -467,15 +470,18 @@ kf_status step_impl(const void *q, const void *k_new, const void *v_new, void *k
     a.v_new = static_cast<const uint16_t *>(v_new);
     a.k_cache = k_cache;
     a.v_cache = v_cache;
-    a.ws_o = num_splits > 1 ? reinterpret_cast<float *>(ws) : nullptr;
-    a.ws_lse = num_splits > 1 ? reinterpret_cast<float *>(ws + al((size_t)num_splits * rows * head_dim * 4)) : nullptr;
-    a.counters = num_splits > 1 ? reinterpret_cast<unsigned int *>(
+    a.ws_o = counted ? reinterpret_cast<float *>(ws) : nullptr;
+    a.ws_lse = counted ? reinterpret_cast<float *>(ws + al((size_t)num_splits * rows * head_dim * 4)) : nullptr;
+    a.counters = counted ? reinterpret_cast<unsigned int *>(
                                       ws + al((size_t)num_splits * rows * head_dim * 4) +
                                       al((size_t)num_splits * rows * 4))
                                 : nullptr;
     a.out = out;
     a.lse_out = lse_out;
     a.out_dtype = (int)out_dtype;
+    a.ex_o = n_ex > 0 ? ex_o : nullptr;
+    a.ex_lse = n_ex > 0 ? ex_lse : nullptr;
+    a.n_ex = n_ex;
     void *fn = encode_fn();
     if (!fn) return KF_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -497,7 +503,25 @@ kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, vo
     return step_impl(q, k_new, v_new, k_cache, v_cache, block_tables, bt_stride,
                      context_lens_before, max_context_len, batch, num_q_heads, num_kv_heads,
                      head_dim, block_size, num_blocks, scale, num_splits, workspace,
-                     workspace_bytes, out, out_dtype, lse_out, nullptr, nullptr, false, stream);
+                     workspace_bytes, out, out_dtype, lse_out, nullptr, nullptr, false, nullptr,
+                     nullptr, 0, stream);
+}
+
+kf_status kf_decode_step_merge_partials(const void *q, const void *k_new, const void *v_new,
+                                        void *k_cache, void *v_cache, const int32_t *block_tables,
+                                        int bt_stride, const int32_t *context_lens_before,
+                                        int max_context_len, int batch, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int64_t num_blocks, float scale, int num_splits,
+                                        const float *extra_out_partial,
+                                        const float *extra_lse_partial, int num_extra,
+                                        void *workspace, size_t workspace_bytes, void *out,
+                                        kf_dtype out_dtype, float *lse_out, kf_stream_t stream) {
+    return step_impl(q, k_new, v_new, k_cache, v_cache, block_tables, bt_stride,
+                     context_lens_before, max_context_len, batch, num_q_heads, num_kv_heads,
+                     head_dim, block_size, num_blocks, scale, num_splits, workspace,
+                     workspace_bytes, out, out_dtype, lse_out, nullptr, nullptr, false,
+                     extra_out_partial, extra_lse_partial, num_extra, stream);
 }
 
 kf_status kf_decode_step_fp8(const void *q, const void *k_new, const void *v_new, void *k_cache,
@@ -511,7 +535,8 @@ kf_status kf_decode_step_fp8(const void *q, const void *k_new, const void *v_new
     return step_impl(q, k_new, v_new, k_cache, v_cache, block_tables, bt_stride,
                      context_lens_before, max_context_len, batch, num_q_heads, num_kv_heads,
                      head_dim, block_size, num_blocks, scale, num_splits, workspace,
-                     workspace_bytes, out, out_dtype, lse_out, k_scale, v_scale, true, stream);
+                     workspace_bytes, out, out_dtype, lse_out, k_scale, v_scale, true, nullptr,
+                     nullptr, 0, stream);
 }
 
 }  // extern "C"

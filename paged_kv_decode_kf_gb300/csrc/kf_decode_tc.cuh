@@ -182,6 +182,9 @@ struct StepParams {
     void *out;               // final [B, Hq, D] (f32 or bf16)
     float *lse_out;          // final [B, Hq], or null
     int out_dtype;
+    const float *ex_o;       // extra partials, merged with the splits': [n_ex, B, Hq, D]
+    const float *ex_lse;     //                                         [n_ex, B, Hq]
+    int n_ex;
 };
 
 // Shared-memory geometry. bf16 caches: boxes of 64 elements (128-byte rows),
@@ -266,15 +269,19 @@ __device__ __forceinline__ int nonempty_splits(const DecodeParams &p, int64_t L)
 // kernel). Uses the shared-memory ring, which is idle by now.
 template <int D, int R>
 __device__ void merge_group(const DecodeParams &p, const StepParams &sp, int b, int row_first,
-                            int n_ne, float *sm) {
+                            int n_sp, float *sm) {
+    // partial s < n_sp is a split's (workspace), s >= n_sp the extra slot s - n_sp
+    const int n_ne = n_sp + sp.n_ex;
     const int64_t rows = (int64_t)p.batch * p.num_q_heads;
+    auto lse_of = [&](int s) { return s < n_sp ? sp.ws_lse + (int64_t)s * rows : sp.ex_lse + (int64_t)(s - n_sp) * rows; };
+    auto o_of = [&](int s) { return s < n_sp ? sp.ws_o + (int64_t)s * rows * D : sp.ex_o + (int64_t)(s - n_sp) * rows * D; };
     float *sm_w = sm;                 // [n_ne][R] lse, then weights
     float *sm_m = sm + n_ne * R;      // [R] row max
     float *sm_sum = sm_m + R;         // [R] sum of weights
     const int nt = blockDim.x, tid = threadIdx.x;
     for (int i = tid; i < n_ne * R; i += nt) {
         const int s = i / R, r = i % R;
-        sm_w[i] = __ldcg(sp.ws_lse + (int64_t)s * rows + (int64_t)b * p.num_q_heads + row_first + r);
+        sm_w[i] = __ldcg(lse_of(s) + (int64_t)b * p.num_q_heads + row_first + r);
     }
     __syncthreads();
     for (int r = tid; r < R; r += nt) {
@@ -282,7 +289,7 @@ __device__ void merge_group(const DecodeParams &p, const StepParams &sp, int b, 
         for (int s = 0; s < n_ne; ++s) M = fmaxf(M, sm_w[s * R + r]);
         float sum = 0.f;
         for (int s = 0; s < n_ne; ++s) {
-            const float w = expf(sm_w[s * R + r] - M);
+            const float w = sm_w[s * R + r] == -INFINITY ? 0.f : expf(sm_w[s * R + r] - M);
             sm_w[s * R + r] = w;
             sum += w;
         }
@@ -312,9 +319,8 @@ __device__ void merge_group(const DecodeParams &p, const StepParams &sp, int b, 
 #pragma unroll
                 for (int k = 0; k < U; ++k) {
                     const int u = u0 + k * nt;
-                    o[j][k] = (live[k] && s0 + j < n_ne)
-                                  ? __ldcg(reinterpret_cast<const float4 *>(
-                                               sp.ws_o + ((int64_t)(s0 + j) * rows + rowu[k]) * D) + u % C)
+                    o[j][k] = (live[k] && s0 + j < n_ne && sm_w[(s0 + j) * R + u / C] != 0.f)
+                                  ? __ldcg(reinterpret_cast<const float4 *>(o_of(s0 + j) + rowu[k] * D) + u % C)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
@@ -720,7 +726,7 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
             const float lse0 = (m_run[0] + log2f(l_acc[0])) * 0.6931471805599453f;
             const float lse1 = (m_run[1] + log2f(l_acc[1])) * 0.6931471805599453f;
             // destination: the partial slot, or (fused, single split) the final rows
-            const bool direct = FUSED && n_ne == 1;
+            const bool direct = FUSED && n_ne == 1 && sp.n_ex == 0;
             const int64_t prow = direct ? (int64_t)b * Hq + (int64_t)hq
                                         : row0 + (int64_t)warp * G;  // row of query head n = 0
             float *o_dst = FUSED ? (direct ? nullptr : sp.ws_o) : p.out_partial;
@@ -773,7 +779,9 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
     }
 
     // ----------------------- fused: count, last CTA merges -----------------------
-    if (FUSED && n_ne > 1) {
+    // (with extra partials even a request of one non-empty split merges: its
+    // single CTA counts itself as the last)
+    if (FUSED && n_ne + sp.n_ex > 1) {
         __shared__ int sm_last;
         __threadfence();  // this CTA's partial is visible before the count
         __syncthreads();
@@ -930,6 +938,9 @@ inline StepParams step_params(const StepArgs &a) {
     sp.out = a.out;
     sp.lse_out = a.lse_out;
     sp.out_dtype = a.out_dtype;
+    sp.ex_o = a.ex_o;
+    sp.ex_lse = a.ex_lse;
+    sp.n_ex = a.n_ex;
     return sp;
 }
 

@@ -46,6 +46,9 @@ struct StepArgs {
     void *out;               // [B, Hq, D] of out_dtype
     float *lse_out;          // [B, Hq] or null
     int out_dtype;
+    const float *ex_o;       // extra partials merged in: [n_ex, B, Hq, D] (or null)
+    const float *ex_lse;     //                           [n_ex, B, Hq]
+    int n_ex;
 };
 
 // Parameters of one multi-query (chunked prefill / shared prefix) launch.

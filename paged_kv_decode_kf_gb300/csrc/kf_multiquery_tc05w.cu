@@ -78,6 +78,7 @@ struct WShape {
     __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + (uint32_t)D * t; }
     // one CTA per SM, so the 512-column allocation always succeeds
     static_assert(kSmemBytes > 116 * 1024 && kSmemBytes <= 227 * 1024, "one CTA per SM");
+    static_assert(2 * kRowsW * D * 4 <= kSlots * kSlotBytes, "the ring holds both tiles' output rows");
 };
 
 template <int D, int G>
@@ -89,8 +90,8 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     constexpr int KS = D / 16;  // K steps of S = Q K^T
     constexpr int KP = kTileW / 16;  // K steps of O += P V
 
-    // barriers: full[NSL], empty[NSL], q_ready, fin, s_full[2], p_full[2]
-    __shared__ __align__(8) uint64_t bar_mem[2 * NSL + 6];
+    // barriers: full[NSL], empty[NSL], q_ready, fin, s_full[2], p_full[2], staged[2]
+    __shared__ __align__(8) uint64_t bar_mem[2 * NSL + 8];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int abort_flag;
     extern __shared__ uint8_t smem_raw[];
@@ -102,6 +103,7 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     const uint32_t q_ready = bars + 8u * (2 * NSL), fin = q_ready + 8;
     auto s_full = [&](int t) { return fin + 8u + 8u * t; };
     auto p_full = [&](int t) { return fin + 24u + 8u * t; };
+    auto staged = [&](int t) { return fin + 40u + 8u * t; };
 
     const int s = blockIdx.x, h = blockIdx.y;
     const int b = blockIdx.z / p.q_tiles, qg = blockIdx.z % p.q_tiles;
@@ -167,6 +169,7 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
         for (int t = 0; t < 2; ++t) {
             mbar_init(s_full(t), 1);
             mbar_init(p_full(t), kRowsW);
+            mbar_init(staged(t), kRowsW);
         }
         abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -416,23 +419,51 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
                 mbar_arrive(p_full(tq));
             }
             if (ok && warp_wait(fin, 0)) {
+                // Epilogue through shared memory (the KV ring is idle once every MMA
+                // is done): each thread writes its normalised O row with 16-byte
+                // chunks XOR-swizzled by row, then each warp copies whole rows out,
+                // one coalesced 16-byte chunk per lane.
                 tc05::fence_after_sync();
+                constexpr int CH = D / 4;                       // 16-byte chunks per row
+                const uint32_t stage = sKV + tq * (kRowsW * D * 4);
                 const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
                     tc05::tmem_ld32(tm + lane_base + col_o + 32 * cc, o);
-                    if (row_ok) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4 *>(o_row + 32 * cc + i) =
-                                l > 0.f ? make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
-                                                      __uint_as_float(o[i + 2]) * inv,
-                                                      __uint_as_float(o[i + 3]) * inv)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int i = 0; i < 8; ++i) {
+                        const int k = 8 * cc + i;
+                        float4 v = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                               __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+                        if (!(l > 0.f)) v = make_float4(0.f, 0.f, 0.f, 0.f);
+                        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                         stage + r * (D * 4) + ((k ^ (r & (CH - 1))) << 4)),
+                                     "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                                     : "memory");
                     }
                 }
                 if (row_ok) *lse_row = l > 0.f ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+                // this tile's rows are staged (a bounded wait: a warp that gave up
+                // earlier never arrives)
+                mbar_arrive(staged(tq));
+                if (!warp_wait(staged(tq), 0)) {
+                    if (r == 0) raise_error(p.err, KF_DEVERR_TIMEOUT);
+                } else
+                for (int rr = warp & 3; rr < kRowsW; rr += 4) {
+                    const int64_t grow = row0 + (int64_t)tq * kRowsW + rr;
+                    if (grow >= nrow_all) break;  // rows ascend: the rest are past the request
+                    float *dst = p.out_partial +
+                                 (((int64_t)s * p.num_q_tokens + q0 + grow / G) * Hq + h * G + (int)(grow % G)) * D;
+                    for (int k = lane; k < CH; k += 32) {
+                        float4 v;
+                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                                     : "r"(stage + rr * (D * 4) + ((k ^ (rr & (CH - 1))) << 4))
+                                     : "memory");
+                        reinterpret_cast<float4 *>(dst)[k] = v;
+                    }
+                }
             } else {
                 if (r == 0) raise_error(p.err, KF_DEVERR_TIMEOUT);
                 abort_flag = 1;

@@ -55,6 +55,10 @@ _lib.kf_decode_step.restype = _i32
 _lib.kf_decode_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32,
                                 _i32, _i64, _f32, _i32, _vp, ctypes.c_size_t, _vp, _i32, _vp, _vp]
 _lib.kf_decode_step_static.restype = _i32
+_lib.kf_decode_step_merge_partials.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
+                                                _i32, _i32, _i64, _f32, _i32, _vp, _vp, _i32, _vp,
+                                                ctypes.c_size_t, _vp, _i32, _vp, _vp]
+_lib.kf_decode_step_merge_partials.restype = _i32
 _lib.kf_decode_step_static.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32,
                                        _i32, _i32, _i64, _f32, _i32, _vp, _i32, _vp, _vp]
 KF_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -265,6 +269,41 @@ def kf_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_
         bs, nb, float(scale), int(num_splits), ws_ptr, ws_bytes, _dev(out, out.dtype, "out"), code,
         None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
         "kf_decode_step")
+    return out, lse_out
+
+
+def kf_decode_step_merge_partials(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                  k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                  context_lens_before: torch.Tensor, max_context_len: int, scale: float,
+                                  num_splits: int, extra_out_partial: torch.Tensor,
+                                  extra_lse_partial: torch.Tensor, workspace: torch.Tensor,
+                                  out: Optional[torch.Tensor] = None, out_dtype=torch.float32,
+                                  lse_out: Optional[torch.Tensor] = None, want_lse: bool = True,
+                                  stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """kf_decode_step whose merge also takes the extra partials
+    ([n, B, Hq, D] and [n, B, Hq]); returns (out, lse)."""
+    B, hq, d = q.shape
+    nb, bs, hkv, d2 = k_cache.shape
+    n_ex = int(extra_lse_partial.shape[0])
+    if tuple(extra_out_partial.shape) != (n_ex, B, hq, d) or tuple(extra_lse_partial.shape) != (n_ex, B, hq):
+        raise ValueError("extra partials must be [n, B, Hq, D] and [n, B, Hq]")
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
+    code = {torch.float32: KF_F32, torch.bfloat16: KF_BF16}.get(out.dtype)
+    if code is None:
+        raise ValueError("out must be float32 or bfloat16")
+    if lse_out is None and want_lse:
+        lse_out = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+    _check(_lib.kf_decode_step_merge_partials(
+        _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
+        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _dev(context_lens_before, torch.int32, "context_lens_before"), int(max_context_len), B, hq, hkv, d,
+        bs, nb, float(scale), int(num_splits), _dev(extra_out_partial, torch.float32, "extra_out_partial"),
+        _dev(extra_lse_partial, torch.float32, "extra_lse_partial"), n_ex,
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _dev(out, out.dtype, "out"), code,
+        None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
+        "kf_decode_step_merge_partials")
     return out, lse_out
 
 

@@ -124,7 +124,7 @@ class CascadeStep:
     sets of partials."""
 
     def __init__(self, inp: DecodeInputs, prefix_splits: Optional[int] = None,
-                 suffix_splits: Optional[int] = None, out_dtype=torch.float32):
+                 suffix_splits: Optional[int] = None, out_dtype=torch.float32, fused_suffix: bool = True):
         w = inp.workload
         assert w.shared_prefix and inp.prefix_table is not None
         self.inp, self.w = inp, w
@@ -156,6 +156,11 @@ class CascadeStep:
         self.lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
         self.fused = False
         self.with_append = True
+        # fused_suffix: append + suffix attention + merge with the prefix partials
+        # in one kf_decode_step_merge_partials launch (two launches per step);
+        # otherwise four calls (append, prefix, suffix, merge)
+        self.fused_suffix = bool(fused_suffix)
+        self.workspace = kf.make_workspace(B, Hq, w.num_kv_heads, w.head_dim, self.Ss, dev) if fused_suffix else None
 
     def append(self, stream=None) -> None:
         i = self.inp
@@ -182,14 +187,26 @@ class CascadeStep:
     def merge(self, stream=None) -> None:
         kf.kf_merge_partials(self.out_partial, self.lse_partial, self.out, lse_out=self.lse, stream=stream)
 
+    def suffix_step(self, stream=None) -> None:
+        """Append, suffix attention and the merge with the prefix partials, one launch."""
+        i, w, Sp = self.inp, self.w, self.Sp
+        kf.kf_decode_step_merge_partials(i.q, i.k_new, i.v_new, i.k_cache, i.v_cache, i.suffix_tables,
+                                         i.suffix_ctx_before, self.max_suffix, w.scale, self.Ss,
+                                         self.out_partial[:Sp], self.lse_partial[:Sp], self.workspace,
+                                         out=self.out, lse_out=self.lse, stream=stream)
+
     def run(self, stream=None) -> None:
+        if self.fused_suffix:
+            self.prefix(stream)
+            self.suffix_step(stream)
+            return
         self.append(stream)
         self.attention(stream)
         self.merge(stream)
 
     @property
     def launches_per_step(self) -> int:
-        return 4
+        return 2 if self.fused_suffix else 4
 
     @property
     def num_splits(self) -> int:

@@ -157,3 +157,27 @@ def test_decode_step_host_checks(kf):
     big = kf.kf_decode_step_workspace_size(4, 32, 8, 128, 2000)
     assert step(S=2000, wsb=big) == kf.KF_ERR_UNSUPPORTED     # the merge would not fit in shared memory
     assert step(d=96) == kf.KF_ERR_UNSUPPORTED
+
+
+def test_decode_step_merge_partials_host_checks(kf):
+    """The extra-partials step: the host checks of kf_decode_step, plus the
+    extra slots (count, pointers, alignment), the workspace it needs even at
+    one split, and the shared-memory bound on splits + extras."""
+    lib = kf.raw()
+    need1 = kf.kf_decode_step_workspace_size(4, 32, 8, 128, 1)
+
+    def step(**kw):
+        a = dict(q=16, kn=16, vn=16, kc=16, vc=16, bt=16, st=8, ctx=16, mc=100, B=4, hq=32, hkv=8, d=128, bs=16,
+                 nb=64, scale=0.1, S=1, eo=16, el=16, ne=3, ws=16, wsb=need1, out=16, dt=kf.KF_F32, lse=None)
+        a.update(kw)
+        return lib.kf_decode_step_merge_partials(
+            a["q"], a["kn"], a["vn"], a["kc"], a["vc"], a["bt"], a["st"], a["ctx"], a["mc"], a["B"], a["hq"],
+            a["hkv"], a["d"], a["bs"], a["nb"], a["scale"], a["S"], a["eo"], a["el"], a["ne"], a["ws"], a["wsb"],
+            a["out"], a["dt"], a["lse"], None)
+    assert step(B=0) == kf.KF_OK
+    for bad in (dict(ne=-1), dict(eo=None), dict(el=None), dict(eo=8), dict(ws=None), dict(wsb=need1 - 1),
+                dict(kn=None), dict(S=0)):
+        assert step(**bad) == kf.KF_ERR_INVALID, bad
+    big = kf.kf_decode_step_workspace_size(4, 32, 8, 128, 1000)
+    assert step(S=1000, ne=1000, wsb=big) == kf.KF_ERR_UNSUPPORTED   # merge of 2000 partials does not fit
+    assert step(d=96) == kf.KF_ERR_UNSUPPORTED

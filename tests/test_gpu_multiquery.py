@@ -86,15 +86,17 @@ def test_multiquery_shapes(kf, hq, hkv, d, bs, impl):
     check_partials(o_p.cpu().numpy(), l_p.cpu().numpy(), ref_po, ref_pl, "mq shapes")
 
 
+@pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("impl", IMPLS)
-def test_cascade_prefix_plus_suffix(kf, impl):
+def test_cascade_prefix_plus_suffix(kf, impl, fused):
     """Prefix attended once for all requests, merged with each suffix, equals
-    decode attention over each request's full table."""
+    decode attention over each request's full table -- as two launches
+    (prefix pass + kf_decode_step_merge_partials) or four."""
     from paged_kv_decode_kf_gb300.step import CascadeStep
     w = wl.scaled(wl.CONFIGS["cascade"], batch=6, lengths=wl.Fixed((5, 70, 300, 1, 16, 999)))
     dev = wl.make_inputs(w, "cuda")
     hv_k, hv_v = wl.bf16_bits(dev.k_cache), wl.bf16_bits(dev.v_cache)
-    step = CascadeStep(dev)
+    step = CascadeStep(dev, fused_suffix=fused)
     with mq_impl(impl):
         step.run()
     torch.cuda.synchronize()
@@ -133,3 +135,31 @@ def test_cascade_full_size_sampled(kf):
     ref_o, ref_l = oracle.attention(hv.q, k2, v2, hv.tables[0], hv.ctx_after, w.scale)
     check_out(step.out.float().cpu().numpy()[reqs], ref_o, "cascade full out")
     check_lse(step.lse.cpu().numpy()[reqs], ref_l, "cascade full lse")
+
+
+def test_decode_step_merge_partials_extra_slots(kf):
+    """One split plus extra partials (the single work unit counts itself as the
+    last and merges); an extra slot with lse = -inf is skipped without reading
+    its o (NaN here); bf16 output."""
+    from paged_kv_decode_kf_gb300.step import CascadeStep
+    w = wl.scaled(wl.CONFIGS["cascade"], batch=5, lengths=wl.Fixed((40, 3, 200, 17, 64)))
+    dev = wl.make_inputs(w, "cuda")
+    hv = HostView(dev, range(w.batch))
+    step = CascadeStep(dev, suffix_splits=1)
+    step.prefix()
+    Sp = step.Sp
+    B, Hq, D = w.batch, w.num_q_heads, w.head_dim
+    ex_o = torch.cat([step.out_partial[:Sp], torch.full((1, B, Hq, D), float("nan"), device="cuda")])
+    ex_l = torch.cat([step.lse_partial[:Sp], torch.full((1, B, Hq), float("-inf"), device="cuda")])
+    ws = kf.make_workspace(B, Hq, w.num_kv_heads, D, 1)
+    out, lse = kf.kf_decode_step_merge_partials(dev.q, dev.k_new, dev.v_new, dev.k_cache, dev.v_cache,
+                                                dev.suffix_tables, dev.suffix_ctx_before, step.max_suffix, w.scale,
+                                                1, ex_o, ex_l, ws, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    k2, v2 = hv.appended()
+    ref_o, ref_l = oracle.attention(hv.q, k2, v2, hv.tables[0], hv.ctx_after, w.scale)
+    check_out(out.float().cpu().numpy(), ref_o, "merge_partials out")
+    check_lse(lse.cpu().numpy(), ref_l, "merge_partials lse")
+    al = lambda x: (x + 255) // 256 * 256
+    off = al(B * Hq * D * 4) + al(B * Hq * 4)    # workspace: partials (1 split), lse, counters
+    assert int(ws[off:off + B * w.num_kv_heads * 4].view(torch.int32).abs().sum()) == 0, "counters not reset"
