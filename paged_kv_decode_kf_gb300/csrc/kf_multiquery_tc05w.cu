@@ -26,8 +26,8 @@
 //                and writes its 128 weights as bf16 pairs over the first 64
 //                columns of its own scores in TMEM (the O rescale comes after
 //                the weights, when the scores are no longer held in registers).
-//   warp 8       TMA producer: one 5-D box per cache block into a ring of 4
-//                slots (K_j, V_j, K_j+1, V_j+1) of 128 tokens.
+//   warp 8       TMA producer: one 5-D box per cache block into a ring of
+//                128-token slots (5 at D = 128), K_j, V_j, K_j+1, ... in turn.
 //   warp 9       MMA issuer and TMEM owner. Per KV tile j and query tile t:
 //                  O_t += P_t V_{j-1}   (A = P_t from TMEM, B = V, MN-major)
 //                  S_t  = Q_t K_j^T     (A = Q_t, B = K, both K-major smem)
@@ -69,7 +69,9 @@ struct WShape {
     static constexpr int kQBytes = 2 * kQTileBytes;
     static constexpr int kAtomBytes = kHalves * 1024;            // 8 tokens x D
     static constexpr int kSlotBytes = kTileW / 8 * kAtomBytes;   // 128 tokens x D
-    static constexpr int kSlots = D == 128 ? 4 : 8;
+    // ring: two slots feed the MMAs while the rest load (TMA latency under load
+    // is about a microsecond, a tile's MMAs take under one): 5 x 32 KiB at D 128
+    static constexpr int kSlots = D == 128 ? 5 : 12;
     static constexpr int kSmemBytes = kQBytes + kSlots * kSlotBytes + 1024;
     static constexpr int kThreads = 320;
     static constexpr int kProducer = 8, kIssuer = 9;
@@ -159,6 +161,22 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     }
     const int ntiles = (int)((t_hi - t_lo + kTileW - 1) / kTileW);
 
+    // Start the producer's first loads before the setup below: the two tensor
+    // maps' descriptors and the first 32 block-table entries (a cold first TMA
+    // issue otherwise waits on both).
+    const int bs_shift = block_shift(p.block_size);
+    int64_t tab_base = -1;
+    int32_t tab_ent = -1;
+    if (warp == Sh::kProducer) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
+        }
+        tab_base = t_lo >> bs_shift;
+        const int64_t e = tab_base + lane;
+        tab_ent = e < p.bt_stride ? p.block_tables[(int64_t)b * p.bt_stride + e] : -1;
+    }
+
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSL; ++i) {
             mbar_init(full(i), 1);
@@ -184,10 +202,7 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
         // The whole warp walks the tiles: table entries come 32 at a time (one
         // coalesced load, lane e holds logical block base + e); lane 0 waits
         // for slots and lane k issues the box of the tile's block k.
-        const int bs_shift = block_shift(p.block_size);
         const uint32_t box_bytes = (uint32_t)p.block_size * D * 2;
-        int64_t tab_base = -1;
-        int32_t tab_ent = -1;
         int issued = 0;
         for (int i = 0; i < 2 * ntiles; ++i) {
             const int slot = i % NSL;
