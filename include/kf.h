@@ -302,7 +302,7 @@ kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, vo
  *
  *   extra_out_partial  f32 [num_extra, batch, num_q_heads, head_dim], 16-byte aligned
  *   extra_lse_partial  f32 [num_extra, batch, num_q_heads]; -inf marks an empty
- *                      slot (its o is not read)
+ *                      slot (its o may hold any bits: it is ignored)
  *   num_extra          >= 0; 0 is kf_decode_step
  *   workspace          as kf_decode_step, and required whenever num_extra > 0
  *                      (the merge counts its work units there even at num_splits = 1)

@@ -274,7 +274,6 @@ __device__ void merge_group(const DecodeParams &p, const StepParams &sp, int b, 
     const int n_ne = n_sp + sp.n_ex;
     const int64_t rows = (int64_t)p.batch * p.num_q_heads;
     auto lse_of = [&](int s) { return s < n_sp ? sp.ws_lse + (int64_t)s * rows : sp.ex_lse + (int64_t)(s - n_sp) * rows; };
-    auto o_of = [&](int s) { return s < n_sp ? sp.ws_o + (int64_t)s * rows * D : sp.ex_o + (int64_t)(s - n_sp) * rows * D; };
     float *sm_w = sm;                 // [n_ne][R] lse, then weights
     float *sm_m = sm + n_ne * R;      // [R] row max
     float *sm_sum = sm_m + R;         // [R] sum of weights
@@ -312,29 +311,39 @@ __device__ void merge_group(const DecodeParams &p, const StepParams &sp, int b, 
             rowu[k] = (int64_t)b * p.num_q_heads + row_first + (live[k] ? u / C : 0);
             acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        for (int s0 = 0; s0 < n_ne; s0 += SB) {
-            float4 o[SB][U];
+        // partials [first, first + n) at `obase` (workspace or extra slots); their
+        // weights sit at sm_w[(w0 + s) * R + row]
+        auto accumulate = [&](const float *obase, int n, int w0) {
+            for (int s0 = 0; s0 < n; s0 += SB) {
+                float4 o[SB][U];
 #pragma unroll
-            for (int j = 0; j < SB; ++j)
+                for (int j = 0; j < SB; ++j)
 #pragma unroll
-                for (int k = 0; k < U; ++k) {
-                    const int u = u0 + k * nt;
-                    o[j][k] = (live[k] && s0 + j < n_ne && sm_w[(s0 + j) * R + u / C] != 0.f)
-                                  ? __ldcg(reinterpret_cast<const float4 *>(o_of(s0 + j) + rowu[k] * D) + u % C)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+                    for (int k = 0; k < U; ++k) {
+                        const int u = u0 + k * nt;
+                        o[j][k] = (live[k] && s0 + j < n)
+                                      ? __ldcg(reinterpret_cast<const float4 *>(
+                                                   obase + ((int64_t)(s0 + j) * rows + rowu[k]) * D) + u % C)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
 #pragma unroll
-            for (int j = 0; j < SB; ++j)
+                for (int j = 0; j < SB; ++j)
 #pragma unroll
-                for (int k = 0; k < U; ++k) {
-                    const int u = u0 + k * nt;
-                    const float w = (live[k] && s0 + j < n_ne) ? sm_w[(s0 + j) * R + u / C] : 0.f;
-                    acc[k].x = fmaf(w, o[j][k].x, acc[k].x);
-                    acc[k].y = fmaf(w, o[j][k].y, acc[k].y);
-                    acc[k].z = fmaf(w, o[j][k].z, acc[k].z);
-                    acc[k].w = fmaf(w, o[j][k].w, acc[k].w);
-                }
-        }
+                    for (int k = 0; k < U; ++k) {
+                        const int u = u0 + k * nt;
+                        const float w = (live[k] && s0 + j < n) ? sm_w[(w0 + s0 + j) * R + u / C] : 0.f;
+                        // a zero weight (an empty extra slot) drops o whatever its bits
+                        if (w != 0.f) {
+                            acc[k].x = fmaf(w, o[j][k].x, acc[k].x);
+                            acc[k].y = fmaf(w, o[j][k].y, acc[k].y);
+                            acc[k].z = fmaf(w, o[j][k].z, acc[k].z);
+                            acc[k].w = fmaf(w, o[j][k].w, acc[k].w);
+                        }
+                    }
+            }
+        };
+        accumulate(sp.ws_o, n_sp, 0);
+        if (sp.n_ex > 0) accumulate(sp.ex_o, sp.n_ex, n_sp);
 #pragma unroll
         for (int k = 0; k < U; ++k) {
             if (!live[k]) continue;
@@ -363,7 +372,9 @@ __device__ void merge_group(const DecodeParams &p, const StepParams &sp, int b, 
 // a request with one non-empty split writes its final rows directly, others
 // go through the workspace and the last CTA merges.
 template <int D, int HPC, int G, int NS, bool FUSED, bool KV8>
-__global__ void __launch_bounds__(TcShape<D, HPC, NS, KV8>::kThreads)
+// (FP8 caches with up to 4 KV heads per CTA: three CTAs per SM is the design --
+// a 64 KiB ring each -- so registers are capped for it)
+__global__ void __launch_bounds__(TcShape<D, HPC, NS, KV8>::kThreads, (KV8 && HPC <= 4) ? 3 : 1)
 decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v) {
     using Sh = TcShape<D, HPC, NS, KV8>;
