@@ -222,6 +222,18 @@ def oracle_sample(w, target_s: float):
     dt = max(time.time() - t, 1e-4)
     tok_per_s = float(pi.ctx_after.sum()) / dt
     budget = tok_per_s * target_s
+    if w.chunk:
+        # chunked prefill: one request and the last `c` queries of its chunk (their
+        # causal limits are those of the full chunk's last c queries), each query
+        # attending to about L tokens
+        b = int(np.random.default_rng(w.seed).integers(w.batch))
+        L = int(lay.ctx_after[b])
+        c = max(1, min(w.chunk, int(budget // L)))
+        sample = wl.Workload(name=w.name + "-sample", batch=1, num_q_heads=w.num_q_heads,
+                             num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, block_size=w.block_size,
+                             lengths=wl.Fixed((int(lay.ctx_before[b]),)), seed=w.seed + 7919, chunk=c,
+                             description=w.description)
+        return sample, threads
     order = np.random.default_rng(w.seed).permutation(w.batch)
     chosen, tot = [], 0
     for b in order:
@@ -237,10 +249,27 @@ def oracle_sample(w, target_s: float):
 def run_oracle_step(si, threads):
     import oracle
     from paged_kv_decode_kf_gb300 import workloads as wl
+    if si.workload.chunk:
+        # causal chunk query j of c over L tokens = attention over its first
+        # L - c + j + 1 tokens: the c queries as c requests sharing the table,
+        # through the threaded decode oracle
+        import numpy as np
+        c, L = si.workload.chunk, int(si.ctx_after[0])
+        bt = np.repeat(si.block_tables.numpy()[:1], c, axis=0)
+        lim = (L - c + 1 + np.arange(c)).astype(np.int32)
+        return oracle.attention(wl.bf16_bits(si.q_chunk), wl.bf16_bits(si.k_cache), wl.bf16_bits(si.v_cache),
+                                bt, lim, si.workload.scale, threads=threads)
     k2, v2, _ = oracle.append(wl.bf16_bits(si.k_cache), wl.bf16_bits(si.v_cache), wl.bf16_bits(si.k_new),
                               wl.bf16_bits(si.v_new), si.block_tables.numpy(), si.ctx_before.numpy())
     return oracle.attention(wl.bf16_bits(si.q), k2, v2, si.block_tables.numpy(), si.ctx_after.numpy(),
                             si.workload.scale, threads=threads)
+
+
+def sample_kv_bytes(si, w) -> float:
+    """KV bytes a sample stands for, in the GPU line's unit: a chunked-prefill
+    sample computes c of its request's C chunk queries, so c/C of its KV."""
+    kv = float(si.kv_bytes())
+    return kv * si.workload.chunk / w.chunk if w.chunk else kv
 
 
 def cpu_baseline(w, target_s=12.0):
@@ -255,7 +284,7 @@ def cpu_baseline(w, target_s=12.0):
         dt = time.time() - t
         if dt >= target_s or passes >= 1000:
             break
-    kv = si.kv_bytes()
+    kv = sample_kv_bytes(si, w)
     return {"value": kv * passes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": "%d of %d requests of the %s workload (%d tokens, %.2f GB of KV); %d append + "
                       "attention passes in fp64 C over all query heads, %.1f s"
@@ -279,7 +308,7 @@ def run_reference(args):
     for _ in range(K):
         run_oracle_step(si, threads)
     dt = (time.time() - t) / max(K, 1)
-    kv = si.kv_bytes()
+    kv = sample_kv_bytes(si, w)
     value = kv / dt / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
@@ -323,14 +352,19 @@ def run_ours(args):
     W = max(args.warmup, 3)
     dev = wl.make_inputs(w, "cuda:%d" % local)
     fused = args.path == "fused" or (args.path == "auto" and not w.shards and not w.shared_prefix
-                                     and args.decode_kernel == "tc")
+                                     and not w.chunk and args.decode_kernel == "tc")
     if w.kv_dtype == "fp8" and args.decode_kernel != "tc":
         raise SystemExit("the FP8 cache is served by the tensor-core kernel only")
     cascade = bool(w.shared_prefix) and args.path in ("auto", "cascade", "cascade-calls")
+    chunk = bool(w.chunk)
     if cascade:
         from paged_kv_decode_kf_gb300.step import CascadeStep
         step = CascadeStep(dev, fused_suffix=args.path != "cascade-calls")
         kv_bytes = step.unique_kv_bytes()      # the prefix once, each suffix once
+    elif chunk:
+        from paged_kv_decode_kf_gb300.step import ChunkStep
+        step = ChunkStep(dev, num_splits=args.num_splits)
+        kv_bytes = dev.kv_bytes()              # each request's cached tokens, once
     else:
         step = DecodeStep(dev, num_splits=args.num_splits, fused=fused)
         kv_bytes = dev.kv_bytes()
@@ -418,7 +452,8 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         names = ["q", "k_new", "v_new", "ctx_before", "ctx_after", "block_tables"]
-        for extra in ("prefix_table", "suffix_tables", "suffix_ctx_before", "suffix_ctx_after"):
+        for extra in ("prefix_table", "suffix_tables", "suffix_ctx_before", "suffix_ctx_after", "q_chunk",
+                      "q_start"):
             if getattr(dev, extra) is not None:
                 names.append(extra)
         tensors = [getattr(dev, n) for n in names]
@@ -450,6 +485,8 @@ def run_ours(args):
                 setattr(dev, n, v)
         if cascade:
             step_e = CascadeStep(dev, prefix_splits=step.Sp, suffix_splits=step.Ss, fused_suffix=step.fused_suffix)
+        elif chunk:
+            step_e = ChunkStep(dev, num_splits=step.S)
         else:
             step_e = DecodeStep(dev, num_splits=step.num_splits, fused=step.fused)
         ob = step_e.out.numel() * step_e.out.element_size()
@@ -510,6 +547,17 @@ def run_ours(args):
                                                                  else ", of fallback"))(
                                      tsrc if pre_s >= suf_s else peak_src),
                                  kernels=kernels)
+    elif chunk:
+        # a dense contraction (every chunk query against its history and the
+        # causal part of its chunk): the bf16 tensor roofline
+        tpk, tsrc = tensor_peak()
+        tf = step.flops() / (att_ms * 1e-3) / 1e12
+        roofline_override = {"bound": "tensor", "achieved": tf, "peak": tpk, "unit": "TFLOP/s", "frac": tf / tpk,
+                             "traffic": None, "algorithmic_flops_per_launch": step.flops(),
+                             "kernel": "multi-query attention (chunk queries, causal)",
+                             "avg_launch_us": att_ms * 1e3, "merge_us": (ms - att_ms) * 1e3,
+                             "peak_source": tsrc + (", of measured" if tsrc.startswith("measured")
+                                                    else ", of fallback")}
     else:
         roofline_override = None
     per_launch_kv = kv_bytes / n_att
@@ -542,12 +590,14 @@ def run_ours(args):
                        "kv_bytes_per_step": kv_bytes, "decode_kernel": args.decode_kernel,
                        "heads_per_cta_override": os.environ.get("KF_TC_HPC"),
                        "num_splits_source": "planner" if args.num_splits is None else "--num-splits",
-                       "step": "append + split attention + LSE merge",
+                       "step": ("chunk attention (multi-query, causal) + LSE merge" if chunk else
+                                "append + split attention + LSE merge"),
                        "path": "kf_decode_step (one launch)" if step.fused else
                                ("kf_paged_multiquery_attention (prefix, once) + kf_decode_step_merge_partials "
                                 "(append + suffixes + merge)" if step.fused_suffix else
                                 "kf_append_kv + kf_paged_multiquery_attention (prefix, once) + "
                                 "kf_paged_decode_attention (suffixes) + kf_merge_partials") if cascade else
+                               "kf_paged_multiquery_attention (causal chunks) + kf_merge_partials" if chunk else
                                "kf_append_kv + kf_paged_decode_attention x%d + kf_merge_partials" % n_att,
                        "logical_kv_bytes_per_step": logical_kv_bytes,
                        "effective_gbs": logical_kv_bytes / (ms * 1e-3) / 1e9,

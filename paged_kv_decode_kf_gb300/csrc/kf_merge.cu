@@ -57,6 +57,24 @@ merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_par
     if (row >= rows) return;
     const int lane = threadIdx.x & 31;
 
+    if (S == 1) {
+        // one partial: the merge is the identity (w = 1); lse and o load together
+        const float l = __ldg(lse_part + row);
+        T o = __ldg(reinterpret_cast<const T *>(o_part + row * D) + lane);
+        if (l == -INFINITY) o = MV::zero();
+        const float *a = reinterpret_cast<const float *>(&o);
+        if (out_dtype == KF_F32) {
+            reinterpret_cast<T *>(static_cast<float *>(out) + row * D)[lane] = o;
+        } else {
+            uint16_t *o16 = static_cast<uint16_t *>(out) + row * D + V * lane;
+#pragma unroll
+            for (int i = 0; i < V; i += 2)
+                *reinterpret_cast<__nv_bfloat162 *>(o16 + i) = __floats2bfloat162_rn(a[i], a[i + 1]);
+        }
+        if (lse_out != nullptr && lane == 0) lse_out[row] = l;
+        return;
+    }
+
     // 1. M = max_s lse_s
     float M = -INFINITY;
     for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldg(lse_part + (int64_t)s * rows + row));

@@ -230,3 +230,67 @@ class CascadeStep:
         tok = self.P + int(self.inp.suffix_ctx_after.to(torch.int64).sum().item())
         return tok * w.kv_bytes_per_token()
 
+
+
+class ChunkStep:
+    """Chunked prefill of one attention layer: every request's newest `chunk`
+    cached tokens are queries that attend to the request's paged history and
+    causally to the chunk (query j of a chunk of C over L cached tokens attends
+    to tokens [0, L - C + j]; "Mathematical Formulation of Chunked Attention",
+    ultrainstinct.tech). One kf_paged_multiquery_attention call (the library
+    picks the kernel by rows per KV head) and one kf_merge_partials."""
+
+    def __init__(self, inp: DecodeInputs, num_splits: Optional[int] = None, out_dtype=torch.float32):
+        w = inp.workload
+        assert w.chunk and inp.q_chunk is not None
+        self.inp, self.w = inp, w
+        dev = inp.q_chunk.device
+        self.C = int(w.chunk)
+        self.N = w.batch * self.C
+        self.max_ctx = int(inp.ctx_after.max().item())
+        if num_splits is None:
+            # about one wave of CTAs: KV heads x requests x 256-row query groups x splits
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            units = w.num_kv_heads * w.batch * max(1, -(-self.C * w.group // 256))
+            num_splits = max(1, min(self.max_ctx // w.block_size, sms // units if units < sms else 1))
+        self.S = int(num_splits)
+        Hq, D = w.num_q_heads, w.head_dim
+        self.out_partial = torch.empty((self.S, self.N, Hq, D), dtype=torch.float32, device=dev)
+        self.lse_partial = torch.empty((self.S, self.N, Hq), dtype=torch.float32, device=dev)
+        self.out = torch.empty((self.N, Hq, D), dtype=out_dtype, device=dev)
+        self.lse = torch.empty((self.N, Hq), dtype=torch.float32, device=dev)
+        self.fused = False
+        self.with_append = False
+
+    def attention(self, stream=None) -> None:
+        i, w = self.inp, self.w
+        kf.kf_paged_multiquery_attention(i.q_chunk, i.q_start, i.k_cache, i.v_cache, i.block_tables, i.ctx_after,
+                                         True, self.max_ctx, self.C, w.scale, self.S, self.out_partial,
+                                         self.lse_partial, stream)
+
+    def merge(self, stream=None) -> None:
+        kf.kf_merge_partials(self.out_partial, self.lse_partial, self.out, lse_out=self.lse, stream=stream)
+
+    def run(self, stream=None) -> None:
+        self.attention(stream)
+        self.merge(stream)
+
+    @property
+    def launches_per_step(self) -> int:
+        return 2
+
+    @property
+    def num_splits(self) -> int:
+        return self.S
+
+    @property
+    def views(self):
+        return [None]
+
+    def flops(self) -> float:
+        """Algorithmic FLOPs: 4 D per (attended token, query row); query j of a
+        chunk of C over L tokens attends to L - C + j + 1 tokens."""
+        w, C = self.w, self.C
+        L = self.inp.ctx_after.to(torch.int64).cpu()
+        tokens = int((C * (L - C) + C * (C + 1) // 2).sum())
+        return 4.0 * w.head_dim * w.num_q_heads * tokens

@@ -119,6 +119,8 @@ class Workload:
     kv_dtype: str = "bf16"         # "bf16" or "fp8" (E4M3 codes with per-KV-head scales)
     shared_prefix: int = 0         # >0: every request starts with these many shared tokens
                                    # (whole blocks); `lengths` then draws the private suffixes
+    chunk: int = 0                 # >0: the last `chunk` cached tokens of each request are a
+                                   # prefill chunk whose queries attend causally (multi-query)
 
     @property
     def group(self) -> int:
@@ -170,6 +172,15 @@ CONFIGS["cascade"] = Workload(
     description="shared-prefix batch: 64 requests behind one 16K-token prefix, private suffixes "
                 "U[64,2048], 32/8 heads, D 128, bs 16")
 
+# Chunked prefill (multi-query, causal): each request's newest `chunk` tokens are
+# in the cache and their queries attend to the paged history and causally to
+# the chunk, not one of the five configs.
+CONFIGS["chunk"] = Workload(
+    name="chunk", batch=4, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+    lengths=Uniform(4096, 12288), seed=1006, chunk=1024,
+    description="chunked prefill: 4 requests, each a causal 1024-token chunk at the end of "
+                "U[4K,12K] cached tokens, 32/8 heads, D 128, bs 16")
+
 CONFIG_ORDER = ("tiny", "llama8b", "longctx", "shard4", "ragged")
 
 
@@ -185,7 +196,7 @@ def scaled(w: Workload, *, batch: Optional[int] = None, lengths=None, name=None,
         seed=seed if seed is not None else w.seed + 7919,
         spare_blocks=w.spare_blocks if spare_blocks is None else spare_blocks,
         num_splits=w.num_splits, shards=w.shards, description=w.description,
-        kv_dtype=kv_dtype or w.kv_dtype, shared_prefix=w.shared_prefix)
+        kv_dtype=kv_dtype or w.kv_dtype, shared_prefix=w.shared_prefix, chunk=w.chunk)
 
 
 def with_kv_dtype(w: Workload, kv_dtype: str) -> Workload:
@@ -194,7 +205,7 @@ def with_kv_dtype(w: Workload, kv_dtype: str) -> Workload:
                     head_dim=w.head_dim, block_size=w.block_size, lengths=w.lengths, seed=w.seed,
                     spare_blocks=w.spare_blocks, num_splits=w.num_splits, shards=w.shards,
                     description=w.description + ("" if kv_dtype == "bf16" else ", FP8 E4M3 KV cache"),
-                    kv_dtype=kv_dtype, shared_prefix=w.shared_prefix)
+                    kv_dtype=kv_dtype, shared_prefix=w.shared_prefix, chunk=w.chunk)
 
 
 def fp8_scales(num_kv_heads: int):
@@ -233,6 +244,9 @@ class DecodeInputs:
     suffix_tables: Optional[torch.Tensor] = field(default=None, kw_only=True)
     suffix_ctx_before: Optional[torch.Tensor] = field(default=None, kw_only=True)
     suffix_ctx_after: Optional[torch.Tensor] = field(default=None, kw_only=True)
+    # ... chunked prefill: the chunk queries [B * chunk, Hq, D] and their row starts [B + 1]
+    q_chunk: Optional[torch.Tensor] = field(default=None, kw_only=True)
+    q_start: Optional[torch.Tensor] = field(default=None, kw_only=True)
     ctx_before: torch.Tensor
     ctx_after: torch.Tensor
     num_blocks: int
@@ -413,6 +427,12 @@ def make_inputs(w: Workload, device="cpu", lengths: Optional[Sequence[int]] = No
         inp.suffix_tables = i32(lay.suffix_tables)
         inp.suffix_ctx_before = i32(lay.suffix_ctx_before)
         inp.suffix_ctx_after = i32(lay.suffix_ctx_before + 1)
+    if w.chunk:
+        # drawn after everything else, so the other inputs do not depend on it;
+        # the chunk is the last `chunk` of each request's ctx_after tokens
+        assert int(lay.ctx_after.min()) >= w.chunk, "every context must hold the chunk"
+        inp.q_chunk = _bf16_normal((B * w.chunk, H, D), gen, dev)
+        inp.q_start = i32(np.arange(B + 1) * w.chunk)
     return inp
 
 

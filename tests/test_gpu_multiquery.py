@@ -163,3 +163,29 @@ def test_decode_step_merge_partials_extra_slots(kf):
     al = lambda x: (x + 255) // 256 * 256
     off = al(B * Hq * D * 4) + al(B * Hq * 4)    # workspace: partials (1 split), lse, counters
     assert int(ws[off:off + B * w.num_kv_heads * 4].view(torch.int32).abs().sum()) == 0, "counters not reset"
+
+
+def test_chunk_full_size_sampled(kf):
+    """The chunked-prefill workload at full size (4 requests, 1024 causal chunk
+    queries each over U[4K,12K] cached tokens: 4096 rows per KV head, the wide
+    tcgen05 kernel) in the configuration the benchmark times; queries at the
+    chunk's start, middle and end against the oracle over their own limits."""
+    from paged_kv_decode_kf_gb300.step import ChunkStep
+    w = wl.CONFIGS["chunk"]
+    dev = wl.make_inputs(w, "cuda")
+    step = ChunkStep(dev)
+    step.run()
+    torch.cuda.synchronize()
+    C = w.chunk
+    reqs = [0, w.batch - 1]
+    hv = HostView(dev, reqs)
+    for idx, b in enumerate(reqs):
+        L = int(hv.ctx_after[idx])
+        js = [0, 1, C // 2, C - 2, C - 1]
+        rows = [b * C + j for j in js]
+        q = wl.bf16_bits(dev.q_chunk[rows])
+        bt = np.repeat(hv.tables[0][idx:idx + 1], len(js), axis=0)
+        lim = np.array([L - C + j + 1 for j in js], np.int32)
+        ref_o, ref_l = oracle.attention(q, hv.k, hv.v, bt, lim, w.scale)
+        check_out(step.out[rows].cpu().numpy(), ref_o, "chunk out, request %d" % b)
+        check_lse(step.lse[rows].cpu().numpy(), ref_l, "chunk lse, request %d" % b)

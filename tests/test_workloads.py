@@ -1,6 +1,7 @@
 """Host-side input recipe: lengths, tables, shard slices (CPU only)."""
 import numpy as np
 import pytest
+import torch
 
 from paged_kv_decode_kf_gb300 import workloads as wl
 
@@ -71,3 +72,20 @@ def test_shard_slices(lengths):
         p = int(lay.tail_ctx_before[b])
         g = int(lay.ctx_before[b])
         assert lay.tail_tables[b, p // bs] == lay.block_tables[b, g // bs] and p % bs == g % bs
+
+
+def test_chunk_inputs():
+    """Chunked prefill: B * chunk query rows drawn after every other input (the
+    cache, q and new rows are those of the same workload without a chunk), row
+    starts at multiples of the chunk, every context at least one chunk long."""
+    w = wl.scaled(wl.CONFIGS["chunk"], batch=3, lengths=wl.Fixed((1100, 2047, 5000)))
+    i = wl.make_inputs(w, "cpu")
+    assert tuple(i.q_chunk.shape) == (3 * w.chunk, w.num_q_heads, w.head_dim)
+    assert i.q_start.tolist() == [0, w.chunk, 2 * w.chunk, 3 * w.chunk]
+    assert int(i.ctx_after.min()) >= w.chunk
+    import dataclasses
+    plain = wl.make_inputs(dataclasses.replace(w, chunk=0), "cpu")
+    assert plain.q_chunk is None
+    assert torch.equal(plain.k_cache, i.k_cache) and torch.equal(plain.q, i.q)
+    lay = wl.plan_layout(wl.CONFIGS["chunk"])
+    assert int(lay.ctx_after.min()) >= wl.CONFIGS["chunk"].chunk
