@@ -112,6 +112,23 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hq = p.num_q_heads;
 
+    // The producer's first loads go out before anything waits on the request's
+    // lengths: the two tensor maps' descriptors and the 32 block-table entries
+    // from the split's first block (both independent of the lengths; a cold
+    // first TMA issue otherwise waits on them).
+    const int bs_shift = block_shift(p.block_size);
+    int64_t tab_base = -1;
+    int32_t tab_ent = -1;
+    if (warp == Sh::kProducer) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
+        }
+        tab_base = ((int64_t)s * p.chunk_blocks * p.block_size) >> bs_shift;
+        const int64_t e = tab_base + lane;
+        tab_ent = e < p.bt_stride ? __ldg(p.block_tables + (int64_t)b * p.bt_stride + e) : -1;
+    }
+
     const int q0 = p.q_start[b], q1 = p.q_start[b + 1];
     if (q0 < 0 || q1 < q0 || q1 > p.num_q_tokens) {  // rows outside q: touch nothing
         if (threadIdx.x == 0 && s == 0 && h == 0 && qg == 0) raise_error(p.err, KF_DEVERR_CONTEXT_LEN);
@@ -160,22 +177,6 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
         return;
     }
     const int ntiles = (int)((t_hi - t_lo + kTileW - 1) / kTileW);
-
-    // Start the producer's first loads before the setup below: the two tensor
-    // maps' descriptors and the first 32 block-table entries (a cold first TMA
-    // issue otherwise waits on both).
-    const int bs_shift = block_shift(p.block_size);
-    int64_t tab_base = -1;
-    int32_t tab_ent = -1;
-    if (warp == Sh::kProducer) {
-        if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
-        }
-        tab_base = t_lo >> bs_shift;
-        const int64_t e = tab_base + lane;
-        tab_ent = e < p.bt_stride ? p.block_tables[(int64_t)b * p.bt_stride + e] : -1;
-    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSL; ++i) {
