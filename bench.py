@@ -53,7 +53,8 @@ def parse():
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
                     help="cache element type (fp8 = E4M3 codes with per-KV-head scales)")
     ap.add_argument("--num-splits", type=int, default=None,
-                    help="override the planner's split count (tuning sweeps)")
+                    help="override the planner's split count (tuning sweeps); 0 = the balanced one-wave "
+                         "schedule of the single-launch step (fused and cascade paths)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -359,7 +360,7 @@ def run_ours(args):
     chunk = bool(w.chunk)
     if cascade:
         from paged_kv_decode_kf_gb300.step import CascadeStep
-        step = CascadeStep(dev, fused_suffix=args.path != "cascade-calls")
+        step = CascadeStep(dev, suffix_splits=args.num_splits, fused_suffix=args.path != "cascade-calls")
         kv_bytes = step.unique_kv_bytes()      # the prefix once, each suffix once
     elif chunk:
         from paged_kv_decode_kf_gb300.step import ChunkStep

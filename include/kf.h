@@ -263,6 +263,8 @@ kf_status kf_merge_partials(const float *out_partial, const float *lse_partial,
  *
  *   context_lens_before  int32 [batch], tokens cached before this step (>= 0)
  *   max_context_len      host-side upper bound of context_lens_before + 1
+ *   num_splits           >= 1 (the split rule, c from max_context_len), or
+ *                        KF_SPLITS_BALANCED (below)
  *   workspace            device scratch of kf_decode_step_workspace_size() bytes,
  *                        16-byte aligned, ZERO-FILLED before its first use; every
  *                        completed call leaves its counters at zero again. Calls
@@ -271,11 +273,34 @@ kf_status kf_merge_partials(const float *out_partial, const float *lse_partial,
  *   out                  [batch, num_q_heads, head_dim] of out_dtype
  *   lse_out              f32 [batch, num_q_heads], or NULL
  *
- * Host errors as kf_paged_decode_attention, plus: a missing or short workspace
- * with num_splits > 1 -> KF_ERR_INVALID; num_splits too large for the merge to
- * fit in the kernel's shared memory -> KF_ERR_UNSUPPORTED.
+ * num_splits = KF_SPLITS_BALANCED (0) replaces the split rule by a balanced
+ * partition of the same tokens (same result up to fp32 rounding order; the
+ * exact merge of KernelFlume section 5.1 holds for any partition): the
+ * 16-token stages of all requests, laid end to end in request order, are cut
+ * into P equal runs, one per CTA, where P x ceil(num_kv_heads / H) is the
+ * number of CTAs the GPU holds at once (H = KV heads per CTA, chosen by the
+ * library); a run may span several requests. Every CTA then does the same
+ * work, so the step takes one even wave whatever the batch's length mix. It
+ * always needs the workspace, of kf_decode_step_workspace_size(..., 0) bytes
+ * on the current device.
+ *
+ * Host errors as kf_paged_decode_attention, plus: num_splits < 0; a missing or
+ * short workspace with num_splits > 1 or num_splits == 0 -> KF_ERR_INVALID;
+ * num_splits too large for the merge to fit in the kernel's shared memory ->
+ * KF_ERR_UNSUPPORTED.
  * Device errors: KF_DEVERR_BLOCK_ID, KF_DEVERR_CONTEXT_LEN (negative length),
  * KF_DEVERR_APPEND_POS (no room in the table), KF_DEVERR_MAX_CONTEXT.
+ */
+#define KF_SPLITS_BALANCED 0
+
+/*
+ * kf_decode_step_workspace_size -- workspace bytes of the kf_decode_step
+ * calls (bf16 and FP8 caches alike). num_splits >= 1: partials
+ * [num_splits, batch, num_q_heads] of head_dim + 1 floats and [batch,
+ * num_kv_heads] counters. num_splits == KF_SPLITS_BALANCED: partial slots of
+ * [num_q_heads, head_dim + 1] floats, two per CTA of the largest one-wave grid
+ * on the CURRENT device plus one per request, and the counters; 0 if that
+ * device cannot be queried or the arguments are invalid.
  */
 size_t kf_decode_step_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                      int num_splits);
@@ -309,8 +334,10 @@ kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, vo
  * Everything else, and the error behaviour, as kf_decode_step, plus:
  * num_extra < 0, or num_extra > 0 with a null or misaligned extra pointer ->
  * KF_ERR_INVALID; num_splits + num_extra too large for the merge to fit in
- * the kernel's shared memory -> KF_ERR_UNSUPPORTED. The extra partials must be
- * complete when the call runs (e.g. written earlier on the same stream).
+ * the kernel's shared memory -> KF_ERR_UNSUPPORTED (the balanced schedule,
+ * num_splits = KF_SPLITS_BALANCED, merges in registers and has no such
+ * limit). The extra partials must be complete when the call runs (e.g.
+ * written earlier on the same stream).
  */
 kf_status kf_decode_step_merge_partials(const void *q, const void *k_new, const void *v_new,
                                         void *k_cache, void *v_cache, const int32_t *block_tables,

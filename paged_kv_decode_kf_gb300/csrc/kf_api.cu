@@ -87,6 +87,38 @@ bool supported_group(int num_q_heads, int num_kv_heads) {
 kf_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KF_OK : KF_ERR_CUDA; }
 
 // ----------------------------------------------------------------------------
+// Balanced schedule of the decode step (num_splits = KF_SPLITS_BALANCED):
+// P CTAs per KV-head group, one wave. Workspace: [batch, Hkv] counters, then
+// 2P + batch partial slots of [Hq, D] o (two per CTA, one per request for a
+// request inside one CTA that merges with extra partials), then as many of
+// [Hq] lse.
+// ----------------------------------------------------------------------------
+struct BalLayout {
+    size_t ctr, o, lse, total;  // byte offsets of the three parts, and the size
+};
+
+BalLayout bal_layout(int ctas, int batch, int num_q_heads, int num_kv_heads, int head_dim) {
+    const auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t slots = 2 * (size_t)ctas + (size_t)batch;
+    BalLayout l;
+    l.ctr = 0;
+    l.o = al((size_t)batch * num_kv_heads * 4);
+    l.lse = l.o + al(slots * num_q_heads * head_dim * 4);
+    l.total = l.lse + al(slots * num_q_heads * 4);
+    return l;
+}
+
+// Upper bound of P over both cache types: CTAs per SM from the kernels'
+// shared memory alone (registers can only lower it), times SMs, per group.
+int bal_ctas_bound(int num_kv_heads, int head_dim, int sm_count) {
+    int hpc = 1, c16 = 1, c8 = 1;
+    decode_tc_shape(num_kv_heads, head_dim, 16, false, &hpc, &c16);
+    decode_tc_shape(num_kv_heads, head_dim, 16, true, &hpc, &c8);
+    const int groups = num_kv_heads / hpc;
+    return std::max(1, std::max(c16, c8) * sm_count / groups);
+}
+
+// ----------------------------------------------------------------------------
 // Split planner: a model of the decode kernel's schedule. Work units are
 // (request, KV-head group, split) CTAs launched split-fastest. While CTAs are
 // still queued, every slot is busy and each CTA streams at the fair share of
@@ -390,7 +422,15 @@ kf_status kf_paged_multiquery_attention(const void *q, const int32_t *q_start, c
 
 size_t kf_decode_step_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                      int num_splits) {
-    if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || num_splits < 1) return 0;
+    if (batch < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || num_splits < 0) return 0;
+    if (num_splits == KF_SPLITS_BALANCED) {
+        if (!supported_dims(head_dim, 16) || !supported_group(num_q_heads, num_kv_heads)) return 0;
+        DeviceInfo *dev = nullptr;
+        if (device_info(&dev) != cudaSuccess) return 0;
+        return bal_layout(bal_ctas_bound(num_kv_heads, head_dim, dev->sm_count), batch, num_q_heads,
+                          num_kv_heads, head_dim)
+            .total;
+    }
     const size_t rows = (size_t)batch * num_q_heads;
     const auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
     return al((size_t)num_splits * rows * head_dim * 4) + al((size_t)num_splits * rows * 4) +
@@ -401,6 +441,95 @@ size_t kf_decode_step_workspace_size(int batch, int num_q_heads, int num_kv_head
 
 namespace {
 
+// Shared DecodeParams of the two step schedules.
+DecodeParams step_decode_params(const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *block_tables, int bt_stride,
+                                const int32_t *context_lens_before, int max_context_len, int batch,
+                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int64_t num_blocks, float scale, int num_splits, const float *k_scale,
+                                const float *v_scale, bool kv8, unsigned int *err) {
+    DecodeParams p;
+    p.q = static_cast<const uint16_t *>(q);
+    p.k_cache = static_cast<const uint16_t *>(k_cache);
+    p.v_cache = static_cast<const uint16_t *>(v_cache);
+    p.block_tables = block_tables;
+    p.ctx_lens = context_lens_before;
+    p.out_partial = nullptr;
+    p.lse_partial = nullptr;
+    p.err = err;
+    p.num_blocks = num_blocks;
+    p.bt_stride = bt_stride;
+    p.max_context_len = max_context_len;
+    p.batch = batch;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.block_size = block_size;
+    p.num_splits = num_splits;
+    const int64_t n_max = ((int64_t)max_context_len + block_size - 1) / block_size;
+    p.chunk_blocks = num_splits > 0 ? (int)std::max<int64_t>(1, (n_max + num_splits - 1) / num_splits) : 1;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.k_scale = kv8 ? k_scale : nullptr;
+    p.v_scale = kv8 ? v_scale : nullptr;
+    return p;
+}
+
+// The decode step on the balanced schedule (arguments checked by step_impl).
+kf_status bal_step(const void *q, const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                   const int32_t *block_tables, int bt_stride, const int32_t *context_lens_before,
+                   int max_context_len, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                   int block_size, int64_t num_blocks, float scale, void *workspace,
+                   size_t workspace_bytes, void *out, kf_dtype out_dtype, float *lse_out,
+                   const float *k_scale, const float *v_scale, bool kv8, const float *ex_o,
+                   const float *ex_lse, int n_ex, kf_stream_t stream) {
+    if (!workspace || !aligned16(workspace)) return KF_ERR_INVALID;
+    DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return KF_ERR_CUDA;
+    int hpc = 1, cps = 1, resident = 0;
+    decode_tc_shape(num_kv_heads, head_dim, block_size, kv8, &hpc, &cps);
+    const cudaError_t re = kv8 ? decode_bal_resident_fp8(head_dim, num_q_heads, num_kv_heads, &resident)
+                               : decode_bal_resident(head_dim, num_q_heads, num_kv_heads, &resident);
+    if (re == cudaErrorInvalidValue) return KF_ERR_UNSUPPORTED;
+    if (re != cudaSuccess) return KF_ERR_CUDA;
+    // one wave; no more CTAs than the batch can have 16-token stages.
+    // KF_BAL_CTAS (CTAs per KV-head group, read per call) overrides it for tuning.
+    int64_t ctas = std::max(1, resident * dev->sm_count / (num_kv_heads / hpc));
+    if (const char *env = getenv("KF_BAL_CTAS")) {
+        const int forced = atoi(env);
+        if (forced > 0) ctas = std::min<int64_t>(forced, bal_ctas_bound(num_kv_heads, head_dim, dev->sm_count));
+    }
+    const int64_t stages_max = (int64_t)batch * (((int64_t)max_context_len + 15) / 16);
+    ctas = std::max<int64_t>(1, std::min(ctas, stages_max));
+    const BalLayout l = bal_layout((int)ctas, batch, num_q_heads, num_kv_heads, head_dim);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < l.total) return KF_ERR_INVALID;
+    const DecodeParams p = step_decode_params(q, k_cache, v_cache, block_tables, bt_stride,
+                                              context_lens_before, max_context_len, batch, num_q_heads,
+                                              num_kv_heads, head_dim, block_size, num_blocks, scale, 0,
+                                              k_scale, v_scale, kv8, dev->err);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    StepArgs a;
+    a.k_new = static_cast<const uint16_t *>(k_new);
+    a.v_new = static_cast<const uint16_t *>(v_new);
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.counters = reinterpret_cast<unsigned int *>(ws + l.ctr);
+    a.ws_o = reinterpret_cast<float *>(ws + l.o);
+    a.ws_lse = reinterpret_cast<float *>(ws + l.lse);
+    a.out = out;
+    a.lse_out = lse_out;
+    a.out_dtype = (int)out_dtype;
+    a.ex_o = n_ex > 0 ? ex_o : nullptr;
+    a.ex_lse = n_ex > 0 ? ex_lse : nullptr;
+    a.n_ex = n_ex;
+    void *fn = encode_fn();
+    if (!fn) return KF_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = kv8 ? launch_decode_step_bal_fp8(p, a, (int)ctas, st, fn)
+                              : launch_decode_step_bal(p, a, (int)ctas, st, fn);
+    if (e == cudaErrorInvalidValue) return KF_ERR_UNSUPPORTED;
+    return from_cuda(e);
+}
+
 kf_status step_impl(const void *q, const void *k_new, const void *v_new, void *k_cache,
                     void *v_cache, const int32_t *block_tables, int bt_stride,
                     const int32_t *context_lens_before, int max_context_len, int batch,
@@ -409,7 +538,7 @@ kf_status step_impl(const void *q, const void *k_new, const void *v_new, void *k
                     size_t workspace_bytes, void *out, kf_dtype out_dtype, float *lse_out,
                     const float *k_scale, const float *v_scale, bool kv8, const float *ex_o,
                     const float *ex_lse, int n_ex, kf_stream_t stream) {
-    if (batch < 0 || num_splits < 1 || bt_stride < 1 || num_blocks < 1 || max_context_len < 0 ||
+    if (batch < 0 || num_splits < 0 || bt_stride < 1 || num_blocks < 1 || max_context_len < 0 ||
         num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || !isfinite(scale) ||
         (out_dtype != KF_BF16 && out_dtype != KF_F32) || n_ex < 0)
         return KF_ERR_INVALID;
@@ -424,6 +553,11 @@ kf_status step_impl(const void *q, const void *k_new, const void *v_new, void *k
     if (!supported_dims(head_dim, block_size) || !supported_group(num_q_heads, num_kv_heads))
         return KF_ERR_UNSUPPORTED;
     if (batch > 65535 || num_splits > 65535) return KF_ERR_UNSUPPORTED;
+    if (num_splits == KF_SPLITS_BALANCED)
+        return bal_step(q, k_new, v_new, k_cache, v_cache, block_tables, bt_stride, context_lens_before,
+                        max_context_len, batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                        num_blocks, scale, workspace, workspace_bytes, out, out_dtype, lse_out, k_scale,
+                        v_scale, kv8, ex_o, ex_lse, n_ex, stream);
     const size_t need = kf_decode_step_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
                                                       num_splits);
     const bool counted = num_splits > 1 || n_ex > 0;  // some group merges: counters needed

@@ -366,6 +366,315 @@ __device__ void merge_group(const DecodeParams &p, const StepParams &sp, int b, 
     }
 }
 
+// ---------------------------------------------------------------------------
+// Consumer-warp pieces (one warp = one KV head and its G query heads), shared
+// by the split-rule kernel below and the balanced-schedule kernel
+// ---------------------------------------------------------------------------
+
+// Q^T of the warp's G query heads as B fragments, in two steps so that the
+// loads can be issued early: load_q_raw reads this lane's words of query head
+// g = lane/4 of the group (q_row; read only for g < G, rows g >= G are zero)
+// into qb as bf16 pairs, b0 = Q[g][16ks + 2qd .. +1], b1 = Q[g][16ks + 8 +
+// 2qd .. +1]; FP8 caches take the k index of a step to d = 16ks + 4qd +
+// {0,1} / {2,3} (the order in which ldmatrix delivers the cache bytes; see
+// stage_math). prep_q then, for FP8 caches, scales q by an exact power of two
+// 2^qe that puts the warp's largest |q| in [2^14, 2^15), so its 8 significant
+// bits are exact in fp16, and returns 2^-qe (1 for bf16).
+template <int D, int G, bool KV8>
+__device__ __forceinline__ void load_q_raw(const uint16_t *q_row, int lane, uint32_t (&qb)[D / 16][2]) {
+    constexpr int KS = D / 16;
+    const int g = lane >> 2, qd = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qb[ks][1] = 0u;
+    if (g < G) {
+        const uint32_t *qrow = reinterpret_cast<const uint32_t *>(q_row);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            if (KV8) {
+                const uint2 v = reinterpret_cast<const uint2 *>(qrow)[4 * ks + qd];
+                qb[ks][0] = v.x;
+                qb[ks][1] = v.y;
+            } else {
+                qb[ks][0] = qrow[8 * ks + qd];
+                qb[ks][1] = qrow[8 * ks + 4 + qd];
+            }
+        }
+    }
+}
+
+template <int D, bool KV8>
+__device__ __forceinline__ float prep_q(uint32_t (&qb)[D / 16][2]) {
+    constexpr int KS = D / 16;
+    float qe_scale = 1.f;
+    if (KV8) {
+        float mx = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+            mx = fmaxf(mx, fmaxf(fmaxf(fabsf(bf16_lo(qb[ks][0])), fabsf(bf16_hi(qb[ks][0]))),
+                                 fmaxf(fabsf(bf16_lo(qb[ks][1])), fabsf(bf16_hi(qb[ks][1])))));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const int qe = (mx > 0.f && isfinite(mx)) ? 14 - ilogbf(mx) : 0;
+        const float up = ldexpf(1.f, qe);
+        qe_scale = ldexpf(1.f, -qe);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qb[ks][0] = pack_f16(bf16_lo(qb[ks][0]) * up, bf16_hi(qb[ks][0]) * up);
+            qb[ks][1] = pack_f16(bf16_lo(qb[ks][1]) * up, bf16_hi(qb[ks][1]) * up);
+        }
+    }
+    return qe_scale;
+}
+
+// The step's append inside a stage: KV head hkv's new K/V row of request b
+// goes to slot t of the stage and to the cache at position p_new (FP8 caches:
+// 16 bf16 values per lane quantised to E4M3 codes of x / scale).
+template <class Sh, int D, bool KV8>
+__device__ __forceinline__ void append_row(const DecodeParams &p, const StepParams &sp, int b, int hkv,
+                                           int64_t p_new, int t, uint32_t kbuf, uint32_t vbuf, int lane) {
+    constexpr int RB = Sh::kRowBytes;
+    constexpr int CH = KV8 ? D / 16 : D / 8;  // 16-byte chunks per row
+    constexpr int CPB = RB / 16;               // chunks per box row
+    if (lane >= 2 * CH) return;
+    const bool is_v = lane >= CH;
+    const int c = is_v ? lane - CH : lane;
+    const uint16_t *src = (is_v ? sp.v_new : sp.k_new) + ((int64_t)b * p.num_kv_heads + hkv) * D;
+    uint4 val;
+    if (KV8) {
+        const float s_q = is_v ? p.v_scale[hkv] : p.k_scale[hkv];
+        const uint4 x0 = reinterpret_cast<const uint4 *>(src)[2 * c];
+        const uint4 x1 = reinterpret_cast<const uint4 *>(src)[2 * c + 1];
+        const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        uint32_t o8[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t lo = f32x2_to_e4m3x2(bf16_lo(w[2 * e]) / s_q, bf16_hi(w[2 * e]) / s_q);
+            const uint32_t hi = f32x2_to_e4m3x2(bf16_lo(w[2 * e + 1]) / s_q, bf16_hi(w[2 * e + 1]) / s_q);
+            o8[e] = lo | (hi << 16);
+        }
+        val = make_uint4(o8[0], o8[1], o8[2], o8[3]);
+    } else {
+        val = reinterpret_cast<const uint4 *>(src)[c];
+    }
+    const uint32_t a = (is_v ? vbuf : kbuf) + (c / CPB) * Sh::kBoxBytes + swz<RB>(t, c % CPB);
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(val.x), "r"(val.y), "r"(val.z),
+                 "r"(val.w)
+                 : "memory");
+    const int64_t phys = physical_block(p, b, p_new / p.block_size);
+    const int64_t off = ((phys * p.block_size + p_new % p.block_size) * p.num_kv_heads + hkv) *
+                        (int64_t)(D * (KV8 ? 1 : 2));  // bytes
+    reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(is_v ? sp.v_cache : sp.k_cache) + off)[c] = val;
+}
+
+// Zero this head's V rows past the end of a partial stage (whole rows, any
+// swizzle): their scores are -inf, but 0 * NaN would still poison O.
+template <class Sh>
+__device__ __forceinline__ void zero_v_tail(uint32_t vbuf, int nvalid, int lane) {
+    constexpr int RB = Sh::kRowBytes;
+    constexpr int CPB = RB / 16;
+    for (int idx = lane; idx < (kTok - nvalid) * CPB * Sh::kHalves; idx += 32) {
+        const int hf = idx / ((kTok - nvalid) * CPB);
+        const int rem = idx % ((kTok - nvalid) * CPB);
+        const int t = nvalid + rem / CPB, c = rem % CPB;
+        const uint32_t a = vbuf + hf * Sh::kBoxBytes + t * RB + c * 16;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
+    }
+}
+
+// One 16-token stage of one warp: S^T = K Q^T, the online-softmax update of
+// (m_run, l_acc, oacc) with tokens >= nvalid masked, and O^T += V^T P^T.
+// kbuf / vbuf are this head's 16 rows of the stage's K and V boxes.
+template <class Sh, int D, bool KV8>
+__device__ __forceinline__ void stage_math(uint32_t kbuf, uint32_t vbuf, int nvalid,
+                                           const uint32_t (&qb)[D / 16][2], float sl2,
+                                           float (&oacc)[D / 16][4], float (&m_run)[2],
+                                           float (&l_acc)[2], int lane) {
+    constexpr int RB = Sh::kRowBytes;
+    constexpr int KS = D / 16;
+    const int g = lane >> 2;
+    const int lj = lane >> 3, lr = lane & 7;  // ldmatrix: matrix lj, row lr
+
+    // S^T = K Q^T : rows = tokens, cols = query heads of the group
+    // two accumulators (even / odd k-steps) halve the dependent MMA chain
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    float sd[4] = {0.f, 0.f, 0.f, 0.f};
+    if (KV8) {
+        // one ldmatrix.x4 = 16 tokens x 32 d codes; each 32-bit register holds 4
+        // consecutive codes of one token, widened to the A fragment of k-step
+        // (low pair -> k 2qd..+1, high pair -> k 2qd+8..+9)
+#pragma unroll
+        for (int kk = 0; kk < KS / 2; ++kk) {
+            const int t = lr + ((lj & 1) << 3);
+            const int chunk = 2 * kk + (lj >> 1);
+            uint32_t fr[4];
+            ldsm_x4(kbuf + swz<RB>(t, chunk), fr);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const uint32_t ra = fr[2 * h2], rb = fr[2 * h2 + 1];
+                const uint32_t af[4] = {e4m3x2_to_f16x2(ra), e4m3x2_to_f16x2(rb),
+                                        e4m3x2_to_f16x2(ra >> 16), e4m3x2_to_f16x2(rb >> 16)};
+                mma_f16(h2 ? sd : sc, af, qb[2 * kk + h2][0], qb[2 * kk + h2][1]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int t = lr + ((lj & 1) << 3);
+            const int chunk = 2 * ks + (lj >> 1);
+            const uint32_t a = kbuf + (chunk >> 3) * Sh::kBoxBytes + swz<128>(t, chunk & 7);
+            uint32_t fr[4];
+            ldsm_x4(a, fr);
+            mma_bf16((ks & 1) ? sd : sc, fr, qb[ks][0], qb[ks][1]);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) sc[e] += sd[e];
+    // scores in base 2, masked past the end; sc[0..1] token g, sc[2..3] token g+8
+    const float x0 = g < nvalid ? sc[0] * sl2 : -INFINITY;
+    const float x1 = g < nvalid ? sc[1] * sl2 : -INFINITY;
+    const float x2 = g + 8 < nvalid ? sc[2] * sl2 : -INFINITY;
+    const float x3 = g + 8 < nvalid ? sc[3] * sl2 : -INFINITY;
+    float mx[2] = {fmaxf(x0, x2), fmaxf(x1, x3)};
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
+        mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        if (mx[j] > m_run[j] + kRescaleSlack) {
+            const float alpha = exp2f(m_run[j] - mx[j]);
+            m_run[j] = mx[j];
+            l_acc[j] *= alpha;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                oacc[mt][j] *= alpha;
+                oacc[mt][j + 2] *= alpha;
+            }
+        }
+    }
+    const float p0 = exp2f(x0 - m_run[0]), p1 = exp2f(x1 - m_run[1]);
+    const float p2 = exp2f(x2 - m_run[0]), p3 = exp2f(x3 - m_run[1]);
+    l_acc[0] += p0 + p2;
+    l_acc[1] += p1 + p3;
+    // P = P_hi + P_lo, both bf16 (fp16 for an FP8 cache): the PV product then
+    // carries ~16 (~22) bits of P
+    uint32_t h01, h23, r01, r23;
+    if (KV8) {
+        h01 = pack_f16(p0, p1);
+        h23 = pack_f16(p2, p3);
+        r01 = pack_f16(p0 - f16_lo(h01), p1 - f16_hi(h01));
+        r23 = pack_f16(p2 - f16_lo(h23), p3 - f16_hi(h23));
+    } else {
+        h01 = pack_bf16(p0, p1);
+        h23 = pack_bf16(p2, p3);
+        r01 = pack_bf16(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
+        r23 = pack_bf16(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
+    }
+    const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);  // P^T, tokens 0-7 / 8-15
+    const uint32_t bl0 = movmatrix_trans(r01), bl1 = movmatrix_trans(r23);
+
+    // O^T += V^T P^T : rows = d, cols = query heads
+    if (KV8) {
+        // V codes: the widened pairs of one token form 8x8 fp16 tiles (rows =
+        // tokens, cols = d 4qd+{0,1} or 4qd+{2,3}); movmatrix.trans turns them into
+        // A fragments whose rows are d in that permuted order
+#pragma unroll
+        for (int mm = 0; mm < KS / 2; ++mm) {
+            const int t = lr + ((lj & 1) << 3);
+            const int chunk = 2 * mm + (lj >> 1);
+            uint32_t fr[4];
+            ldsm_x4(vbuf + swz<RB>(t, chunk), fr);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const uint32_t ra = fr[2 * h2], rb = fr[2 * h2 + 1];
+                const uint32_t af[4] = {movmatrix_trans(e4m3x2_to_f16x2(ra)),
+                                        movmatrix_trans(e4m3x2_to_f16x2(ra >> 16)),
+                                        movmatrix_trans(e4m3x2_to_f16x2(rb)),
+                                        movmatrix_trans(e4m3x2_to_f16x2(rb >> 16))};
+                mma_f16(oacc[2 * mm + h2], af, bh0, bh1);
+                mma_f16(oacc[2 * mm + h2], af, bl0, bl1);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            const int t = lr + ((lj >> 1) << 3);
+            const int chunk = 2 * mt + (lj & 1);
+            const uint32_t a = vbuf + (chunk >> 3) * Sh::kBoxBytes + swz<128>(t, chunk & 7);
+            uint32_t fr[4];
+            ldsm_x4_trans(a, fr);
+            mma_bf16(oacc[mt], fr, bh0, bh1);
+            mma_bf16(oacc[mt], fr, bl0, bl1);
+        }
+    }
+}
+
+// End of a warp's token range: l summed over the 8 token lanes, o = O * vsc / l
+// and lse = (m + log2 l) ln 2 for the G query heads. Rows go to o_dst (f32,
+// row stride D) at row prow + n, or, with o_dst null, to the final output
+// (f32 or bf16); lse to l_dst[prow + n] unless l_dst is null.
+template <int D, int G, bool KV8>
+__device__ __forceinline__ void write_rows(const float (&oacc)[D / 16][4], float (&l_acc)[2],
+                                           const float (&m_run)[2], float vsc, int64_t prow,
+                                           float *o_dst, void *out, int out_dtype, float *l_dst,
+                                           int lane) {
+    constexpr int KS = D / 16;
+    const int g = lane >> 2, qd = lane & 3;
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l_acc[0] += __shfl_xor_sync(0xffffffffu, l_acc[0], off);
+        l_acc[1] += __shfl_xor_sync(0xffffffffu, l_acc[1], off);
+    }
+    const int n0 = 2 * qd, n1 = 2 * qd + 1;
+    const float inv0 = vsc / l_acc[0], inv1 = vsc / l_acc[1];
+    const float lse0 = (m_run[0] + log2f(l_acc[0])) * 0.6931471805599453f;
+    const float lse1 = (m_run[1] + log2f(l_acc[1])) * 0.6931471805599453f;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+        // rows of O^T held by this thread: bf16 path d = 16mt+g and +8; FP8 path
+        // (permuted rows) d = 16mt + 4(g/2) + g%2 and +2
+        const int d0 = KV8 ? 16 * mt + 4 * (g >> 1) + (g & 1) : 16 * mt + g;
+        const int d1 = KV8 ? d0 + 2 : d0 + 8;
+        const float v00 = oacc[mt][0] * inv0, v01 = oacc[mt][2] * inv0;
+        const float v10 = oacc[mt][1] * inv1, v11 = oacc[mt][3] * inv1;
+        if (o_dst != nullptr) {
+            if (n0 < G) {
+                o_dst[(prow + n0) * D + d0] = v00;
+                o_dst[(prow + n0) * D + d1] = v01;
+            }
+            if (n1 < G) {
+                o_dst[(prow + n1) * D + d0] = v10;
+                o_dst[(prow + n1) * D + d1] = v11;
+            }
+        } else if (out_dtype == KF_F32) {
+            float *dst = static_cast<float *>(out);
+            if (n0 < G) {
+                dst[(prow + n0) * D + d0] = v00;
+                dst[(prow + n0) * D + d1] = v01;
+            }
+            if (n1 < G) {
+                dst[(prow + n1) * D + d0] = v10;
+                dst[(prow + n1) * D + d1] = v11;
+            }
+        } else {
+            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(out);
+            if (n0 < G) {
+                dst[(prow + n0) * D + d0] = __float2bfloat16_rn(v00);
+                dst[(prow + n0) * D + d1] = __float2bfloat16_rn(v01);
+            }
+            if (n1 < G) {
+                dst[(prow + n1) * D + d0] = __float2bfloat16_rn(v10);
+                dst[(prow + n1) * D + d1] = __float2bfloat16_rn(v11);
+            }
+        }
+    }
+    if (g == 0 && l_dst != nullptr) {
+        if (n0 < G) l_dst[prow + n0] = lse0;
+        if (n1 < G) l_dst[prow + n1] = lse1;
+    }
+}
+
 // FUSED = false: one split's partial into out_partial (empty split -> 0, -inf).
 // FUSED = true: the whole decode step. ctx_lens are the pre-append lengths;
 // CTAs of empty splits exit at once; the tail split appends the new K/V row;
@@ -478,13 +787,13 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
         if (!FUSED) return;
     } else {
         // ------------------------------- consumers --------------------------------
-        const int g = lane >> 2, qd = lane & 3;
+        const int g = lane >> 2;
+        const int qd = lane & 3;
         const int hkv = h0 + warp;
         const int hq = hkv * G;  // first query head of this warp's KV head
 
-        // Q^T as B fragments: b0 = Q[g][16ks + 2qd .. +1], b1 = Q[g][16ks + 8 + 2qd .. +1]
-        // (FP8: the k index of a step maps to d = 16ks + 4qd + {0,1} / {2,3}, the
-        // order in which ldmatrix delivers the cache bytes; see the QK loop)
+        // Q^T as B fragments, as load_q_raw + prep_q build them (written out here:
+        // as calls the FP8 instantiation with three CTAs per SM spills a register)
         uint32_t qb[KS][2];
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qb[ks][1] = 0u;
@@ -532,9 +841,6 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
         for (int mt = 0; mt < KS; ++mt) oacc[mt][0] = oacc[mt][1] = oacc[mt][2] = oacc[mt][3] = 0.f;
         float m_run[2] = {-INFINITY, -INFINITY};
         float l_acc[2] = {0.f, 0.f};
-
-        // ldmatrix row addresses: lane -> (matrix j = lane/8, row = lane%8)
-        const int lj = lane >> 3, lr = lane & 7;
         const uint32_t head_off = warp * (kTok * RB);  // this head's 16 rows in a box
 
         for (int i = 0; i < n_sub; ++i) {
@@ -550,175 +856,17 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
             const int64_t rem_tok = r.t_end - t_base;
             const int nvalid = rem_tok < kTok ? (int)rem_tok : kTok;
             bool wrote_smem = false;
-
             if (FUSED && p_new >= t_base && p_new < t_base + kTok) {
-                // the step's append: this head's new K/V row into the stage and the cache
-                const int t = (int)(p_new - t_base);
-                constexpr int CH = KV8 ? D / 16 : D / 8;  // 16-byte chunks per row
-                constexpr int CPB = RB / 16;               // chunks per box row
-                if (lane < 2 * CH) {
-                    const bool is_v = lane >= CH;
-                    const int c = is_v ? lane - CH : lane;
-                    const uint16_t *src = (is_v ? sp.v_new : sp.k_new) + ((int64_t)b * p.num_kv_heads + hkv) * D;
-                    uint4 val;
-                    if (KV8) {
-                        // 16 bf16 -> 16 E4M3 codes of x / scale
-                        const float s_q = is_v ? p.v_scale[hkv] : p.k_scale[hkv];
-                        const uint4 x0 = reinterpret_cast<const uint4 *>(src)[2 * c];
-                        const uint4 x1 = reinterpret_cast<const uint4 *>(src)[2 * c + 1];
-                        const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                        uint32_t o8[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint32_t lo = f32x2_to_e4m3x2(bf16_lo(w[2 * e]) / s_q, bf16_hi(w[2 * e]) / s_q);
-                            const uint32_t hi = f32x2_to_e4m3x2(bf16_lo(w[2 * e + 1]) / s_q,
-                                                                bf16_hi(w[2 * e + 1]) / s_q);
-                            o8[e] = lo | (hi << 16);
-                        }
-                        val = make_uint4(o8[0], o8[1], o8[2], o8[3]);
-                    } else {
-                        val = reinterpret_cast<const uint4 *>(src)[c];
-                    }
-                    const uint32_t a = (is_v ? vbuf : kbuf) + (c / CPB) * Sh::kBoxBytes + swz<RB>(t, c % CPB);
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(val.x),
-                                 "r"(val.y), "r"(val.z), "r"(val.w)
-                                 : "memory");
-                    const int64_t phys = physical_block(p, b, p_new / p.block_size);
-                    const int64_t off = ((phys * p.block_size + p_new % p.block_size) * p.num_kv_heads + hkv) *
-                                        (int64_t)(D * (KV8 ? 1 : 2));  // bytes
-                    reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(is_v ? sp.v_cache : sp.k_cache) + off)[c] = val;
-                }
+                append_row<Sh, D, KV8>(p, sp, b, hkv, p_new, (int)(p_new - t_base), kbuf, vbuf, lane);
                 wrote_smem = true;
                 __syncwarp();
             }
             if (nvalid < kTok) {
-                // zero this head's V rows past the end (whole rows, any swizzle)
-                constexpr int CPB = RB / 16;
-                for (int idx = lane; idx < (kTok - nvalid) * CPB * Sh::kHalves; idx += 32) {
-                    const int hf = idx / ((kTok - nvalid) * CPB);
-                    const int rem = idx % ((kTok - nvalid) * CPB);
-                    const int t = nvalid + rem / CPB, c = rem % CPB;
-                    const uint32_t a = vbuf + hf * Sh::kBoxBytes + t * RB + c * 16;
-                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u) : "memory");
-                }
+                zero_v_tail<Sh>(vbuf, nvalid, lane);
                 wrote_smem = true;
                 __syncwarp();
             }
-
-            // S^T = K Q^T : rows = tokens, cols = query heads of the group
-            // two accumulators (even / odd k-steps) halve the dependent MMA chain
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
-            float sd[4] = {0.f, 0.f, 0.f, 0.f};
-            if (KV8) {
-                // one ldmatrix.x4 = 16 tokens x 32 d codes; each 32-bit register holds 4
-                // consecutive codes of one token, widened to the A fragment of k-step
-                // (low pair -> k 2qd..+1, high pair -> k 2qd+8..+9)
-#pragma unroll
-                for (int kk = 0; kk < KS / 2; ++kk) {
-                    const int t = lr + ((lj & 1) << 3);
-                    const int chunk = 2 * kk + (lj >> 1);
-                    uint32_t fr[4];
-                    ldsm_x4(kbuf + swz<RB>(t, chunk), fr);
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const uint32_t ra = fr[2 * h2], rb = fr[2 * h2 + 1];
-                        const uint32_t af[4] = {e4m3x2_to_f16x2(ra), e4m3x2_to_f16x2(rb),
-                                                e4m3x2_to_f16x2(ra >> 16), e4m3x2_to_f16x2(rb >> 16)};
-                        mma_f16(h2 ? sd : sc, af, qb[2 * kk + h2][0], qb[2 * kk + h2][1]);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int t = lr + ((lj & 1) << 3);
-                    const int chunk = 2 * ks + (lj >> 1);
-                    const uint32_t a = kbuf + (chunk >> 3) * Sh::kBoxBytes + swz<128>(t, chunk & 7);
-                    uint32_t fr[4];
-                    ldsm_x4(a, fr);
-                    mma_bf16((ks & 1) ? sd : sc, fr, qb[ks][0], qb[ks][1]);
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sc[e] += sd[e];
-            // scores in base 2, masked past the end; sc[0..1] token g, sc[2..3] token g+8
-            const float x0 = g < nvalid ? sc[0] * sl2 : -INFINITY;
-            const float x1 = g < nvalid ? sc[1] * sl2 : -INFINITY;
-            const float x2 = g + 8 < nvalid ? sc[2] * sl2 : -INFINITY;
-            const float x3 = g + 8 < nvalid ? sc[3] * sl2 : -INFINITY;
-            float mx[2] = {fmaxf(x0, x2), fmaxf(x1, x3)};
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], off));
-                mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], off));
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                if (mx[j] > m_run[j] + kRescaleSlack) {
-                    const float alpha = exp2f(m_run[j] - mx[j]);
-                    m_run[j] = mx[j];
-                    l_acc[j] *= alpha;
-#pragma unroll
-                    for (int mt = 0; mt < KS; ++mt) {
-                        oacc[mt][j] *= alpha;
-                        oacc[mt][j + 2] *= alpha;
-                    }
-                }
-            }
-            const float p0 = exp2f(x0 - m_run[0]), p1 = exp2f(x1 - m_run[1]);
-            const float p2 = exp2f(x2 - m_run[0]), p3 = exp2f(x3 - m_run[1]);
-            l_acc[0] += p0 + p2;
-            l_acc[1] += p1 + p3;
-            // P = P_hi + P_lo, both bf16 (fp16 for an FP8 cache): the PV product then
-            // carries ~16 (~22) bits of P
-            uint32_t h01, h23, r01, r23;
-            if (KV8) {
-                h01 = pack_f16(p0, p1);
-                h23 = pack_f16(p2, p3);
-                r01 = pack_f16(p0 - f16_lo(h01), p1 - f16_hi(h01));
-                r23 = pack_f16(p2 - f16_lo(h23), p3 - f16_hi(h23));
-            } else {
-                h01 = pack_bf16(p0, p1);
-                h23 = pack_bf16(p2, p3);
-                r01 = pack_bf16(p0 - bf16_lo(h01), p1 - bf16_hi(h01));
-                r23 = pack_bf16(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
-            }
-            const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);  // P^T, tokens 0-7 / 8-15
-            const uint32_t bl0 = movmatrix_trans(r01), bl1 = movmatrix_trans(r23);
-
-            // O^T += V^T P^T : rows = d, cols = query heads
-            if (KV8) {
-                // V codes: the widened pairs of one token form 8x8 bf16 tiles
-                // (rows = tokens, cols = d 4qd+{0,1} or 4qd+{2,3}); movmatrix.trans
-                // turns them into A fragments whose rows are d in that permuted order
-#pragma unroll
-                for (int mm = 0; mm < KS / 2; ++mm) {
-                    const int t = lr + ((lj & 1) << 3);
-                    const int chunk = 2 * mm + (lj >> 1);
-                    uint32_t fr[4];
-                    ldsm_x4(vbuf + swz<RB>(t, chunk), fr);
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const uint32_t ra = fr[2 * h2], rb = fr[2 * h2 + 1];
-                        const uint32_t af[4] = {movmatrix_trans(e4m3x2_to_f16x2(ra)),
-                                                movmatrix_trans(e4m3x2_to_f16x2(ra >> 16)),
-                                                movmatrix_trans(e4m3x2_to_f16x2(rb)),
-                                                movmatrix_trans(e4m3x2_to_f16x2(rb >> 16))};
-                        mma_f16(oacc[2 * mm + h2], af, bh0, bh1);
-                        mma_f16(oacc[2 * mm + h2], af, bl0, bl1);
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int mt = 0; mt < KS; ++mt) {
-                    const int t = lr + ((lj >> 1) << 3);
-                    const int chunk = 2 * mt + (lj & 1);
-                    const uint32_t a = vbuf + (chunk >> 3) * Sh::kBoxBytes + swz<128>(t, chunk & 7);
-                    uint32_t fr[4];
-                    ldsm_x4_trans(a, fr);
-                    mma_bf16(oacc[mt], fr, bh0, bh1);
-                    mma_bf16(oacc[mt], fr, bl0, bl1);
-                }
-            }
+            stage_math<Sh, D, KV8>(kbuf, vbuf, nvalid, qb, sl2, oacc, m_run, l_acc, lane);
             // generic smem writes above must be ordered before the next TMA into this stage
             if (wrote_smem) fence_proxy_async_smem();
             __syncwarp();
@@ -726,65 +874,13 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
         }
 
         if (ok) {
-            // finish: l over the 8 token lanes, then o = O / l and lse
-#pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                l_acc[0] += __shfl_xor_sync(0xffffffffu, l_acc[0], off);
-                l_acc[1] += __shfl_xor_sync(0xffffffffu, l_acc[1], off);
-            }
-            const int n0 = 2 * qd, n1 = 2 * qd + 1;
-            const float inv0 = vsc / l_acc[0], inv1 = vsc / l_acc[1];
-            const float lse0 = (m_run[0] + log2f(l_acc[0])) * 0.6931471805599453f;
-            const float lse1 = (m_run[1] + log2f(l_acc[1])) * 0.6931471805599453f;
             // destination: the partial slot, or (fused, single split) the final rows
             const bool direct = FUSED && n_ne == 1 && sp.n_ex == 0;
             const int64_t prow = direct ? (int64_t)b * Hq + (int64_t)hq
                                         : row0 + (int64_t)warp * G;  // row of query head n = 0
             float *o_dst = FUSED ? (direct ? nullptr : sp.ws_o) : p.out_partial;
             float *l_dst = FUSED ? (direct ? sp.lse_out : sp.ws_lse) : p.lse_partial;
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                // rows of O^T held by this thread: bf16 path d = 16mt+g and +8; FP8 path
-                // (permuted rows) d = 16mt + 4(g/2) + g%2 and +2
-                const int d0 = KV8 ? 16 * mt + 4 * (g >> 1) + (g & 1) : 16 * mt + g;
-                const int d1 = KV8 ? d0 + 2 : d0 + 8;
-                const float v00 = oacc[mt][0] * inv0, v01 = oacc[mt][2] * inv0;
-                const float v10 = oacc[mt][1] * inv1, v11 = oacc[mt][3] * inv1;
-                if (o_dst != nullptr) {
-                    if (n0 < G) {
-                        o_dst[(prow + n0) * D + d0] = v00;
-                        o_dst[(prow + n0) * D + d1] = v01;
-                    }
-                    if (n1 < G) {
-                        o_dst[(prow + n1) * D + d0] = v10;
-                        o_dst[(prow + n1) * D + d1] = v11;
-                    }
-                } else if (sp.out_dtype == KF_F32) {
-                    float *out = static_cast<float *>(sp.out);
-                    if (n0 < G) {
-                        out[(prow + n0) * D + d0] = v00;
-                        out[(prow + n0) * D + d1] = v01;
-                    }
-                    if (n1 < G) {
-                        out[(prow + n1) * D + d0] = v10;
-                        out[(prow + n1) * D + d1] = v11;
-                    }
-                } else {
-                    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(sp.out);
-                    if (n0 < G) {
-                        out[(prow + n0) * D + d0] = __float2bfloat16_rn(v00);
-                        out[(prow + n0) * D + d1] = __float2bfloat16_rn(v01);
-                    }
-                    if (n1 < G) {
-                        out[(prow + n1) * D + d0] = __float2bfloat16_rn(v10);
-                        out[(prow + n1) * D + d1] = __float2bfloat16_rn(v11);
-                    }
-                }
-            }
-            if (g == 0 && l_dst != nullptr) {
-                if (n0 < G) l_dst[prow + n0] = lse0;
-                if (n1 < G) l_dst[prow + n1] = lse1;
-            }
+            write_rows<D, G, KV8>(oacc, l_acc, m_run, vsc, prow, o_dst, sp.out, sp.out_dtype, l_dst, lane);
         }
         if (!FUSED) return;
     }

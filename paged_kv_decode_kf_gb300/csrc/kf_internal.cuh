@@ -84,6 +84,15 @@ cudaError_t launch_decode_step_tc(const DecodeParams &p, const StepArgs &a, cuda
 cudaError_t launch_decode_tc_fp8(const DecodeParams &p, cudaStream_t stream, void *encode_fn);
 cudaError_t launch_decode_step_tc_fp8(const DecodeParams &p, const StepArgs &a, cudaStream_t stream,
                                       void *encode_fn);
+// The decode step on the balanced schedule: `ctas` CTAs per KV-head group,
+// one wave (see kf_decode_bal.cuh); StepArgs' workspace pointers hold its
+// layout. *_resident: CTAs of that kernel one SM holds for this shape.
+cudaError_t decode_bal_resident(int head_dim, int num_q_heads, int num_kv_heads, int *resident);
+cudaError_t decode_bal_resident_fp8(int head_dim, int num_q_heads, int num_kv_heads, int *resident);
+cudaError_t launch_decode_step_bal(const DecodeParams &p, const StepArgs &a, int ctas, cudaStream_t stream,
+                                   void *encode_fn);
+cudaError_t launch_decode_step_bal_fp8(const DecodeParams &p, const StepArgs &a, int ctas,
+                                       cudaStream_t stream, void *encode_fn);
 // Bytes of the tensor-core kernel's shared-memory ring (the fused merge reuses it).
 int decode_tc_ring_bytes(int num_kv_heads, int head_dim, bool kv8);
 // Largest number of resident CTAs per SM and KV heads per CTA the tensor-core

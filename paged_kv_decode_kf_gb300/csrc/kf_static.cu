@@ -54,29 +54,33 @@ extern "C" kf_status kf_decode_step_static(
     int max_context_len, int batch, int num_q_heads, int num_kv_heads, int head_dim,
     int block_size, int64_t num_blocks, float scale, int num_splits, void *out,
     kf_dtype out_dtype, float *lse_out, kf_stream_t stream) {
-    if (batch < 0 || num_splits < 1 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1)
+    if (batch < 0 || num_splits < 0 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1)
         return KF_ERR_INVALID;
     if (batch == 0) return KF_OK;
+    const bool uses = num_splits != 1;  // the split rule with S > 1, or the balanced schedule
     const size_t need =
         kf_decode_step_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, num_splits);
-    if (num_splits > 1 && need > (size_t)KF_STATIC_SCRATCH_BYTES) return KF_ERR_UNSUPPORTED;
+    if (uses && need == 0) return num_splits == KF_SPLITS_BALANCED ? KF_ERR_CUDA : KF_ERR_INVALID;
+    if (uses && need > (size_t)KF_STATIC_SCRATCH_BYTES) return KF_ERR_UNSUPPORTED;
     void *scratch = nullptr;
     if (kf::scratch_address(&scratch) != cudaSuccess) return KF_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (num_splits > 1) {
+    if (uses) {
         // the merge counters must start at zero; the array keeps whatever the
-        // previous call left, so clear them on this call's stream
-        const size_t rows = (size_t)batch * num_q_heads;
-        const auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-        const size_t ctr_off = al((size_t)num_splits * rows * head_dim * 4) + al((size_t)num_splits * rows * 4);
+        // previous call left, so clear them on this call's stream (split rule:
+        // after the partials; balanced schedule: at the start)
+        size_t ctr_off = 0;
+        if (num_splits > 1) {
+            const size_t rows = (size_t)batch * num_q_heads;
+            const auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+            ctr_off = al((size_t)num_splits * rows * head_dim * 4) + al((size_t)num_splits * rows * 4);
+        }
         if (cudaMemsetAsync(static_cast<unsigned char *>(scratch) + ctr_off, 0,
                             (size_t)batch * num_kv_heads * 4, st) != cudaSuccess)
             return KF_ERR_CUDA;
     }
     return kf_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, bt_stride,
                           context_lens_before, max_context_len, batch, num_q_heads, num_kv_heads,
-                          head_dim, block_size, num_blocks, scale, num_splits,
-                          num_splits > 1 ? scratch : nullptr,
-                          num_splits > 1 ? (size_t)KF_STATIC_SCRATCH_BYTES : 0, out, out_dtype,
-                          lse_out, stream);
+                          head_dim, block_size, num_blocks, scale, num_splits, uses ? scratch : nullptr,
+                          uses ? (size_t)KF_STATIC_SCRATCH_BYTES : 0, out, out_dtype, lse_out, stream);
 }

@@ -25,6 +25,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 KF_OK, KF_ERR_INVALID, KF_ERR_UNSUPPORTED, KF_ERR_CUDA, KF_ERR_DEVICE = range(5)
 KF_BF16, KF_F32 = 0, 1
+KF_SPLITS_BALANCED = 0  # num_splits of the step calls: balanced one-wave schedule
 KF_DEVERR_BLOCK_ID = 0x01
 KF_DEVERR_CONTEXT_LEN = 0x02
 KF_DEVERR_MAX_CONTEXT = 0x04
@@ -257,8 +258,8 @@ def kf_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_
         raise ValueError("out must be float32 or bfloat16")
     if lse_out is None and want_lse:
         lse_out = torch.empty((B, hq), dtype=torch.float32, device=q.device)
-    if workspace is None and num_splits > 1:
-        raise ValueError("num_splits > 1 needs a workspace (make_workspace)")
+    if workspace is None and num_splits != 1:
+        raise ValueError("num_splits > 1 and the balanced schedule need a workspace (make_workspace)")
     ws_ptr = None if workspace is None else _dev(workspace, torch.uint8, "workspace")
     ws_bytes = 0 if workspace is None else workspace.numel()
     _check(_lib.kf_decode_step(
@@ -386,8 +387,8 @@ def kf_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, bloc
         raise ValueError("out must be float32 or bfloat16")
     if lse_out is None and want_lse:
         lse_out = torch.empty((B, hq), dtype=torch.float32, device=q.device)
-    if workspace is None and num_splits > 1:
-        raise ValueError("num_splits > 1 needs a workspace (make_workspace)")
+    if workspace is None and num_splits != 1:
+        raise ValueError("num_splits > 1 and the balanced schedule need a workspace (make_workspace)")
     _check(_lib.kf_decode_step_fp8(
         _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
         _dev8(k_cache, "k_cache"), _dev8(v_cache, "v_cache"), _dev(k_scale, torch.float32, "k_scale"),

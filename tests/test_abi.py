@@ -7,6 +7,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -140,7 +141,9 @@ def test_decode_step_host_checks(kf):
     al = lambda x: (x + 255) // 256 * 256
     assert need == al(10 * 4 * 32 * 128 * 4) + al(10 * 4 * 32 * 4) + al(4 * 8 * 4)
     assert kf.kf_decode_step_workspace_size(0, 32, 8, 128, 1) == al(0) + al(0) + al(0)
-    assert kf.kf_decode_step_workspace_size(4, 32, 8, 128, 0) == 0
+    assert kf.kf_decode_step_workspace_size(4, 32, 8, 128, -1) == 0
+    if not torch.cuda.is_available():   # the balanced layout is sized for the current device
+        assert kf.kf_decode_step_workspace_size(4, 32, 8, 128, kf.KF_SPLITS_BALANCED) == 0
 
     def step(**kw):
         a = dict(q=16, kn=16, vn=16, kc=16, vc=16, bt=16, st=8, ctx=16, mc=100, B=4, hq=32, hkv=8, d=128, bs=16,
@@ -151,7 +154,7 @@ def test_decode_step_host_checks(kf):
                                   a["wsb"], a["out"], a["dt"], a["lse"], None)
     assert step(B=0) == kf.KF_OK
     for bad in (dict(ws=None), dict(wsb=need - 1), dict(ws=8), dict(kn=None), dict(out=None), dict(dt=3),
-                dict(S=0), dict(mc=-1), dict(scale=float("nan"))):
+                dict(S=-1), dict(mc=-1), dict(scale=float("nan")), dict(S=0, ws=None), dict(S=0, ws=8)):
         assert step(**bad) == kf.KF_ERR_INVALID, bad
     assert step(S=100000) == kf.KF_ERR_UNSUPPORTED
     big = kf.kf_decode_step_workspace_size(4, 32, 8, 128, 2000)
@@ -176,7 +179,7 @@ def test_decode_step_merge_partials_host_checks(kf):
             a["out"], a["dt"], a["lse"], None)
     assert step(B=0) == kf.KF_OK
     for bad in (dict(ne=-1), dict(eo=None), dict(el=None), dict(eo=8), dict(ws=None), dict(wsb=need1 - 1),
-                dict(kn=None), dict(S=0)):
+                dict(kn=None), dict(S=-1), dict(S=0, ws=None)):
         assert step(**bad) == kf.KF_ERR_INVALID, bad
     big = kf.kf_decode_step_workspace_size(4, 32, 8, 128, 1000)
     assert step(S=1000, ne=1000, wsb=big) == kf.KF_ERR_UNSUPPORTED   # merge of 2000 partials does not fit
