@@ -435,6 +435,19 @@ kf_status kf_decode_step_static(const void *q, const void *k_new, const void *v_
  */
 kf_status kf_get_device_error(unsigned int *flags, kf_stream_t stream);
 
+/*
+ * kf_check_bounded_wait -- exercise the timeout path of the kernels' waits.
+ *
+ * The TMA-fed kernels wait on shared-memory mbarriers, each wait bounded: a
+ * wait that gives up sets KF_DEVERR_TIMEOUT in the error word and the kernel
+ * returns instead of hanging. This call launches one block that waits, with
+ * the same bounded wait at a short limit (2^16 polls, milliseconds), on a
+ * barrier that nothing completes, so it always sets KF_DEVERR_TIMEOUT; a
+ * following kf_get_device_error reports it, and the context stays usable.
+ * Returns KF_ERR_CUDA if the launch fails.
+ */
+kf_status kf_check_bounded_wait(kf_stream_t stream);
+
 /* Static description of a status code. */
 const char *kf_status_string(kf_status s);
 

@@ -777,4 +777,10 @@ kf_status kf_get_device_error(unsigned int *flags, kf_stream_t stream) {
     return word ? KF_ERR_DEVICE : KF_OK;
 }
 
+kf_status kf_check_bounded_wait(kf_stream_t stream) {
+    DeviceInfo *dev = nullptr;
+    if (device_info(&dev) != cudaSuccess) return KF_ERR_CUDA;
+    return from_cuda(launch_wait_check(dev->err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -23,6 +23,24 @@ int decode_tc_ring_bytes(int num_kv_heads, int head_dim, bool kv8) {
     return smem - 1024 - 16 * 8;  // minus alignment slack and the largest barrier block
 }
 
+// One wait that nothing completes: an mbarrier expecting one arrival that
+// never comes, polled with the kernels' bounded wait at a short limit (2^16
+// polls); when it gives up, the error word gets KF_DEVERR_TIMEOUT and the
+// kernel returns like the decode kernels do.
+__global__ void wait_check_kernel(unsigned int *err) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = tc::smem_u32(&bar);
+    if (threadIdx.x != 0) return;
+    tc::mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (!tc::mbar_wait(b, 0, 1u << 16)) raise_error(err, KF_DEVERR_TIMEOUT);
+}
+
+cudaError_t launch_wait_check(unsigned int *err, cudaStream_t stream) {
+    wait_check_kernel<<<1, 32, 0, stream>>>(err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode_tc(const DecodeParams &p, cudaStream_t stream, void *encode) {
     tc::StepParams sp = {};
     return tc::launch_any<false, false>(p, sp, stream, encode);

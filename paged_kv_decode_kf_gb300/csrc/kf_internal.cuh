@@ -93,6 +93,8 @@ cudaError_t launch_decode_step_bal(const DecodeParams &p, const StepArgs &a, int
                                    void *encode_fn);
 cudaError_t launch_decode_step_bal_fp8(const DecodeParams &p, const StepArgs &a, int ctas,
                                        cudaStream_t stream, void *encode_fn);
+// One bounded wait that nothing completes (sets KF_DEVERR_TIMEOUT).
+cudaError_t launch_wait_check(unsigned int *err, cudaStream_t stream);
 // Bytes of the tensor-core kernel's shared-memory ring (the fused merge reuses it).
 int decode_tc_ring_bytes(int num_kv_heads, int head_dim, bool kv8);
 // Largest number of resident CTAs per SM and KV heads per CTA the tensor-core

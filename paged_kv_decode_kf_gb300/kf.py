@@ -73,6 +73,8 @@ _lib.kf_decode_step_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32
                                     _i32, _i32, _i32, _i64, _f32, _i32, _vp, ctypes.c_size_t, _vp, _i32, _vp,
                                     _vp]
 _lib.kf_get_device_error.restype = _i32
+_lib.kf_check_bounded_wait.restype = _i32
+_lib.kf_check_bounded_wait.argtypes = [_vp]
 _lib.kf_get_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), _vp]
 _lib.kf_status_string.restype = ctypes.c_char_p
 _lib.kf_status_string.argtypes = [_i32]
@@ -400,6 +402,11 @@ def kf_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, bloc
         None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
         "kf_decode_step_fp8")
     return out, lse_out
+
+
+def kf_check_bounded_wait(stream=None) -> None:
+    """Launch one bounded wait that nothing completes (sets KF_DEVERR_TIMEOUT)."""
+    _check(_lib.kf_check_bounded_wait(_stream(stream)), "kf_check_bounded_wait")
 
 
 def kf_get_device_error(stream=None) -> int:

@@ -143,3 +143,17 @@ def test_device_errors(kf):
     kf.kf_decode_step(dev.q, dev.k_new, dev.v_new, dev.k_cache, dev.v_cache, dev.block_tables, full,
                       int(full.max().item()) + 1, w.scale, 1, None)
     assert kf.kf_get_device_error() & kf.KF_DEVERR_APPEND_POS
+
+
+def test_bounded_wait_gives_up_cleanly(kf):
+    """A wait that nothing completes gives up after its bound, sets
+    KF_DEVERR_TIMEOUT and returns; the context stays usable: a step run right
+    after it matches the oracle."""
+    kf.kf_check_bounded_wait()
+    assert kf.kf_get_device_error() & kf.KF_DEVERR_TIMEOUT
+    assert kf.kf_get_device_error() == 0            # read and cleared
+    w = wl.scaled(wl.CONFIGS["llama8b"], batch=3, lengths=wl.Fixed((40, 300, 17)))
+    dev = wl.make_inputs(w, "cuda")
+    hv = HostView(dev, range(w.batch))
+    out, lse, _ = _fused(kf, dev, 2)
+    _check_against_oracle(dev, hv, out, lse, what="after a timeout")
