@@ -383,26 +383,67 @@ def run_ours(args):
         step.run()
     torch.cuda.synchronize()
 
-    # The single-launch step is capturable (no host synchronisation, no
+    # One step with its phases bracketed by events (recorded on the current
+    # stream): fused: [the launch]; cascade with the fused suffix: prefix pass |
+    # prefix merge | suffix step; cascade as calls: append | prefix | suffix |
+    # merge; otherwise append, [attention] | merge.
+    def one_step(e):
+        if step.fused:
+            e[0].record()
+            step.step_fused()
+            e[1].record()
+            return
+        if cascade:
+            if step.fused_suffix:
+                e[0].record()
+                step.prefix()
+                e[1].record()
+                step.prefix_merge()
+                e[2].record()
+                step.suffix_step()
+                e[3].record()
+                return
+            e[0].record()
+            step.append()
+            e[1].record()
+            step.prefix()
+            e[2].record()
+            step.suffix()
+            e[3].record()
+            step.merge()
+            e[4].record()
+            return
+        if step.with_append:
+            step.append()
+        e[0].record()
+        step.attention()
+        e[1].record()
+        step.merge()
+
+    # Every path's calls are capturable (no host synchronisation, no
     # allocation), so, as a serving loop would, the timed region replays a
     # CUDA graph of n consecutive steps (n the largest divisor of K up to 50):
-    # every replay re-runs all of each step's work, without the host launch
-    # gap between steps.
+    # every replay re-runs all of each step's work, without the host launch gap
+    # between launches. Events inside the graph would serialise it, so the
+    # graph holds the bare steps; per-launch times come from the step time
+    # (one launch per step) or, for paths of several launches, from an
+    # event-timed pass of host-launched steps right after the timed region.
+    def events():
+        return [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+
     graph, g_steps = None, 0
-    if step.fused and not args.no_graph:
+    if not args.no_graph:
         g_steps = max(d for d in range(1, min(K, 50) + 1) if K % d == 0)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for _ in range(g_steps):
-                step.step_fused()
+                step.run()
         graph.replay()
         torch.cuda.synchronize()
 
     # ---- device-timed region ----
     n_att = len(step.views)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    # cascade: append | prefix pass | suffix decode | merge, each bracketed
-    evc = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)] if cascade else None
+    ev = [events() for _ in range(K)] if graph is None else None
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
@@ -413,52 +454,37 @@ def run_ours(args):
     for _ in range(K // g_steps if graph is not None else 0):
         graph.replay()
     for i in range(K if graph is None else 0):
-        if step.fused:
-            ev[i][0].record(stream)
-            step.step_fused()
-            ev[i][1].record(stream)
-            continue
-        if cascade:
-            e = evc[i]
-            if step.fused_suffix:   # prefix pass | suffix step (append + attention + merge)
-                e[0].record(stream)
-                step.prefix()
-                e[1].record(stream)
-                step.suffix_step()
-                e[2].record(stream)
-                continue
-            e[0].record(stream)
-            step.append()
-            e[1].record(stream)
-            step.prefix()
-            e[2].record(stream)
-            step.suffix()
-            e[3].record(stream)
-            step.merge()
-            e[4].record(stream)
-            continue
-        if step.with_append:
-            step.append()
-        ev[i][0].record(stream)
-        step.attention()
-        ev[i][1].record(stream)
-        step.merge()
+        one_step(ev[i])
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
     t1 = time.time()
     clk = clocks.stop(t0, t1)
     ms = start.elapsed_time(end) / K
-    if cascade:
-        nph = 2 if step.fused_suffix else 4
-        phase_ms = [sum(e[k].elapsed_time(e[k + 1]) for e in evc) / K for k in range(nph)]
-        if step.fused_suffix:   # as (append, prefix, suffix, merge) with the fused ones inside "suffix"
-            phase_ms = [0.0, phase_ms[0], phase_ms[1], 0.0]
-        att_ms = phase_ms[1] + phase_ms[2]
+    phase_source = "events in the timed region (host launches)"
+    if graph is not None and not step.fused:
+        # the stream first sleeps (a bounded clock spin) while the host enqueues
+        # every step, so the events see device time, not host launch gaps
+        ev = [events() for _ in range(min(K, 20))]
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(40_000_000)   # ~20 ms at 2 GHz
+        for e in ev:
+            one_step(e)
+        torch.cuda.synchronize()
+        phase_source = "event-timed pass of %d steps enqueued behind a stream sleep, after the timed region" % len(ev)
     elif graph is not None:
-        att_ms = ms    # one launch per step, so the step time bounds the launch time
+        phase_source = "one launch per step: the graph-replayed step time bounds the launch"
+    span = lambda k: sum(e[k].elapsed_time(e[k + 1]) for e in ev) / len(ev)
+    if cascade:
+        if step.fused_suffix:   # as (append, prefix, suffix, merge): the append is inside the suffix step
+            phase_ms = [0.0, span(0), span(2), span(1)]
+        else:
+            phase_ms = [span(k) for k in range(4)]
+        att_ms = phase_ms[1] + phase_ms[2]
+    elif graph is not None and step.fused:
+        att_ms = ms
     else:
-        att_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+        att_ms = span(0)
     from paged_kv_decode_kf_gb300 import kf
     flags = kf.kf_get_device_error()
     if flags:
@@ -552,8 +578,9 @@ def run_ours(args):
         pre_s, suf_s = phase_ms[1] * 1e-3, phase_ms[2] * 1e-3
         pre_tf = step.prefix_flops() / pre_s / 1e12
         suf_gbs = step.suffix_kv_bytes() / suf_s / 1e9
-        kernels = {"path": "2 launches: prefix pass, then kf_decode_step_merge_partials (append + suffix "
-                           "attention + merge with the prefix partials)" if step.fused_suffix else
+        kernels = {"path": "3 launches: prefix pass, merge of its partials into one, then "
+                           "kf_decode_step_merge_partials (append + suffix attention + merge with the "
+                           "prefix partial)" if step.fused_suffix else
                            "4 launches: append, prefix pass, suffix decode, merge",
                    "append_us": phase_ms[0] * 1e3, "prefix_pass_us": phase_ms[1] * 1e3,
                    "suffix_decode_us": phase_ms[2] * 1e3, "merge_us": phase_ms[3] * 1e3,
@@ -616,14 +643,16 @@ def run_ours(args):
                        "step": ("chunk attention (multi-query, causal) + LSE merge" if chunk else
                                 "append + split attention + LSE merge"),
                        "path": "kf_decode_step (one launch)" if step.fused else
-                               ("kf_paged_multiquery_attention (prefix, once) + kf_decode_step_merge_partials "
-                                "(append + suffixes + merge)" if step.fused_suffix else
+                               ("kf_paged_multiquery_attention (prefix, once) + kf_merge_partials (prefix "
+                                "slots into one) + kf_decode_step_merge_partials (append + suffixes + merge)"
+                                if step.fused_suffix else
                                 "kf_append_kv + kf_paged_multiquery_attention (prefix, once) + "
                                 "kf_paged_decode_attention (suffixes) + kf_merge_partials") if cascade else
                                "kf_paged_multiquery_attention (causal chunks) + kf_merge_partials" if chunk else
                                "kf_append_kv + kf_paged_decode_attention x%d + kf_merge_partials" % n_att,
                        "launch": ("CUDA graph replay, %d steps per graph" % g_steps if graph is not None
                                   else "host launches, one step at a time"),
+                       "launch_times": phase_source,
                        "logical_kv_bytes_per_step": logical_kv_bytes,
                        "effective_gbs": logical_kv_bytes / (ms * 1e-3) / 1e9,
                        "l2": "no flush: the %.2f GB of KV read per step exceeds the 129 MB L2" % (kv_bytes / 1e9)
