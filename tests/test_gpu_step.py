@@ -157,3 +157,31 @@ def test_bounded_wait_gives_up_cleanly(kf):
     hv = HostView(dev, range(w.batch))
     out, lse, _ = _fused(kf, dev, 2)
     _check_against_oracle(dev, hv, out, lse, what="after a timeout")
+
+
+@pytest.mark.parametrize("kind", ["fused", "balanced", "cascade", "calls"])
+def test_graph_captured_step_matches_eager(kind):
+    """The step's calls need no host synchronisation and allocate nothing, so
+    they capture into a CUDA graph (as the benchmark replays them): a replay
+    gives the eager step's output and lse bit for bit."""
+    from paged_kv_decode_kf_gb300.step import CascadeStep, DecodeStep
+    if kind == "cascade":
+        w = wl.scaled(wl.CONFIGS["cascade"], batch=6, lengths=wl.Fixed((5, 70, 300, 1, 16, 999)))
+        dev = wl.make_inputs(w, "cuda")
+        step = CascadeStep(dev)
+    else:
+        w = wl.scaled(wl.CONFIGS["ragged"], batch=5, lengths=wl.Fixed((500, 31, 2000, 64, 777)))
+        dev = wl.make_inputs(w, "cuda")
+        step = DecodeStep(dev, num_splits=0 if kind == "balanced" else None, fused=kind != "calls")
+    step.run()
+    torch.cuda.synchronize()
+    ref_o, ref_l = step.out.clone(), step.lse.clone()
+    step.out.zero_()
+    step.lse.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step.run()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(step.out, ref_o) and torch.equal(step.lse, ref_l)
