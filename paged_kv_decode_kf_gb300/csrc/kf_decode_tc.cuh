@@ -49,9 +49,10 @@
 // 2qd+8+e <-> 4qd+2+e), with Q^T's fragments loaded in the same order. V's
 // widened pairs form 8x8 tiles (rows tokens) that movmatrix.trans turns into
 // the A fragment of O^T += V^T P^T with O's rows in a permuted d order,
-// undone when the rows are written. The scales multiply the scores and the
-// output. The fused step quantises the appended row (x / scale, nearest-even,
-// saturating) with cvt.rn.satfinite.e4m3x2.f32.
+// undone when the rows are written; P enters that product as one fp16 value
+// (11 significant bits against bf16's 8, so no P_lo term). The scales
+// multiply the scores and the output. The fused step quantises the appended
+// row (x / scale, nearest-even, saturating) with cvt.rn.satfinite.e4m3x2.f32.
 //
 // Safety: every mbarrier wait is bounded; a wait that gives up sets
 // KF_DEVERR_TIMEOUT and the CTA stops. Out-of-range table entries are
@@ -558,14 +559,14 @@ __device__ __forceinline__ void stage_math(uint32_t kbuf, uint32_t vbuf, int nva
     const float p2 = exp2f(x2 - m_run[0]), p3 = exp2f(x3 - m_run[1]);
     l_acc[0] += p0 + p2;
     l_acc[1] += p1 + p3;
-    // P = P_hi + P_lo, both bf16 (fp16 for an FP8 cache): the PV product then
-    // carries ~16 (~22) bits of P
-    uint32_t h01, h23, r01, r23;
+    // bf16 caches: P = P_hi + P_lo, both bf16, two MMAs: the PV product carries
+    // ~16 bits of P; FP8 caches: P in fp16, one MMA
+    uint32_t h01, h23, r01 = 0u, r23 = 0u;
     if (KV8) {
+        // fp16 P (11 significant bits): one MMA; a weight is off by at most
+        // 2^-11 relative, an output by at most 2^-11 max|v|
         h01 = pack_f16(p0, p1);
         h23 = pack_f16(p2, p3);
-        r01 = pack_f16(p0 - f16_lo(h01), p1 - f16_hi(h01));
-        r23 = pack_f16(p2 - f16_lo(h23), p3 - f16_hi(h23));
     } else {
         h01 = pack_bf16(p0, p1);
         h23 = pack_bf16(p2, p3);
@@ -573,7 +574,7 @@ __device__ __forceinline__ void stage_math(uint32_t kbuf, uint32_t vbuf, int nva
         r23 = pack_bf16(p2 - bf16_lo(h23), p3 - bf16_hi(h23));
     }
     const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);  // P^T, tokens 0-7 / 8-15
-    const uint32_t bl0 = movmatrix_trans(r01), bl1 = movmatrix_trans(r23);
+    const uint32_t bl0 = KV8 ? 0u : movmatrix_trans(r01), bl1 = KV8 ? 0u : movmatrix_trans(r23);
 
     // O^T += V^T P^T : rows = d, cols = query heads
     if (KV8) {
@@ -594,7 +595,6 @@ __device__ __forceinline__ void stage_math(uint32_t kbuf, uint32_t vbuf, int nva
                                         movmatrix_trans(e4m3x2_to_f16x2(rb)),
                                         movmatrix_trans(e4m3x2_to_f16x2(rb >> 16))};
                 mma_f16(oacc[2 * mm + h2], af, bh0, bh1);
-                mma_f16(oacc[2 * mm + h2], af, bl0, bl1);
             }
         }
     } else {
