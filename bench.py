@@ -667,7 +667,9 @@ def run_ours(args):
                                 if step.fused_suffix else
                                 "kf_append_kv + kf_paged_multiquery_attention (prefix, once) + "
                                 "kf_paged_decode_attention (suffixes) + kf_merge_partials") if cascade else
-                               "kf_paged_multiquery_attention (causal chunks) + kf_merge_partials" if chunk else
+                               ("kf_paged_multiquery_attention (causal chunks) + kf_merge_partials" if step.merges
+                                else "kf_paged_multiquery_attention (causal chunks; one split: its partial slot "
+                                     "is the output)") if chunk else
                                "kf_append_kv + kf_paged_decode_attention x%d + kf_merge_partials" % n_att,
                        "launch": ("CUDA graph replay, %d steps per graph" % g_steps if graph is not None
                                   else "host launches, one step at a time"),

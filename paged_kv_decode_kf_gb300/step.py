@@ -253,7 +253,9 @@ class ChunkStep:
     causally to the chunk (query j of a chunk of C over L cached tokens attends
     to tokens [0, L - C + j]; "Mathematical Formulation of Chunked Attention",
     ultrainstinct.tech). One kf_paged_multiquery_attention call (the library
-    picks the kernel by rows per KV head) and one kf_merge_partials."""
+    picks the kernel by rows per KV head) and one kf_merge_partials; with one
+    split and fp32 output the merge of a single partial is the identity (o and
+    lse as they are), so the partial slot is the output and no merge runs."""
 
     def __init__(self, inp: DecodeInputs, num_splits: Optional[int] = None, out_dtype=torch.float32):
         w = inp.workload
@@ -272,8 +274,11 @@ class ChunkStep:
         Hq, D = w.num_q_heads, w.head_dim
         self.out_partial = torch.empty((self.S, self.N, Hq, D), dtype=torch.float32, device=dev)
         self.lse_partial = torch.empty((self.S, self.N, Hq), dtype=torch.float32, device=dev)
-        self.out = torch.empty((self.N, Hq, D), dtype=out_dtype, device=dev)
-        self.lse = torch.empty((self.N, Hq), dtype=torch.float32, device=dev)
+        if self.S == 1 and out_dtype == torch.float32:
+            self.out, self.lse = self.out_partial[0], self.lse_partial[0]
+        else:
+            self.out = torch.empty((self.N, Hq, D), dtype=out_dtype, device=dev)
+            self.lse = torch.empty((self.N, Hq), dtype=torch.float32, device=dev)
         self.fused = False
         self.with_append = False
 
@@ -283,8 +288,15 @@ class ChunkStep:
                                          True, self.max_ctx, self.C, w.scale, self.S, self.out_partial,
                                          self.lse_partial, stream)
 
+    @property
+    def merges(self) -> bool:
+        """False when the output is the single partial slot itself."""
+        return not (self.out.data_ptr() == self.out_partial[0].data_ptr() and
+                    self.lse.data_ptr() == self.lse_partial[0].data_ptr())
+
     def merge(self, stream=None) -> None:
-        kf.kf_merge_partials(self.out_partial, self.lse_partial, self.out, lse_out=self.lse, stream=stream)
+        if self.merges:
+            kf.kf_merge_partials(self.out_partial, self.lse_partial, self.out, lse_out=self.lse, stream=stream)
 
     def run(self, stream=None) -> None:
         self.attention(stream)
@@ -292,7 +304,7 @@ class ChunkStep:
 
     @property
     def launches_per_step(self) -> int:
-        return 2
+        return 2 if self.merges else 1
 
     @property
     def num_splits(self) -> int:
