@@ -183,9 +183,10 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str, kernel: str, kv_bytes_per_launch: float):
+def profiled_traffic(workload: str, kernel: str, kv_bytes_per_launch: float, kv_dtype: str = "bf16"):
     """`kernel` is "tc" (attention launch of the three-call path) or "fused"
-    (the single-launch step)."""
+    (the single-launch step); records of FP8-cache runs are keyed
+    "<workload>_fp8"."""
     path = os.path.join(ROOT, "profiles", "attention_dram_traffic.json")
     if kernel not in ("tc", "fused") or not os.path.exists(path):
         return None
@@ -194,7 +195,8 @@ def profiled_traffic(workload: str, kernel: str, kv_bytes_per_launch: float):
             rec = json.load(f)
         if rec.get("kernel_source_digest") != kernel_source_digest():
             return None
-        per = rec.get("per_workload" if kernel == "tc" else "per_workload_fused", {}).get(workload)
+        key = workload if kv_dtype == "bf16" else workload + "_" + kv_dtype
+        per = rec.get("per_workload" if kernel == "tc" else "per_workload_fused", {}).get(key)
         if per is None:
             return None
         # scaled to one launch of this run by the KV bytes it processes
@@ -630,7 +632,7 @@ def run_ours(args):
     else:
         roofline_override = None
     per_launch_kv = kv_bytes / n_att
-    traffic = profiled_traffic(w.name, "fused" if step.fused else args.decode_kernel, per_launch_kv)
+    traffic = profiled_traffic(w.name, "fused" if step.fused else args.decode_kernel, per_launch_kv, w.kv_dtype)
     kname = ("decode step, one launch (append + attention + merge)" if step.fused
              else "shared-prefix multi-query pass + suffix decode attention" if cascade
              else "decode attention (%s)" % args.decode_kernel)
