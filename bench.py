@@ -65,7 +65,8 @@ def parse():
 
 def default_steps(workload: str) -> int:
     # about one second of timed device work per workload (clock samples land in it)
-    return {"tiny": 2000, "llama8b": 4000, "longctx": 800, "shard4": 800, "ragged": 250}.get(workload, 200)
+    return {"tiny": 2000, "llama8b": 4000, "longctx": 800, "shard4": 800, "ragged": 250, "chunk": 1000,
+            "specverify": 4000, "cascade": 4000}.get(workload, 200)
 
 
 def hbm_peak():
@@ -619,16 +620,26 @@ def run_ours(args):
                                      tsrc if pre_s >= suf_s else peak_src),
                                  kernels=kernels)
     elif chunk:
-        # a dense contraction (every chunk query against its history and the
-        # causal part of its chunk): the bf16 tensor roofline
+        # every chunk query against its history and the causal part of its
+        # chunk: a dense contraction whose bound follows its arithmetic
+        # intensity -- the bf16 tensor roofline for long chunks (prefill),
+        # HBM for a few queries per request (speculative verify)
         tpk, tsrc = tensor_peak()
-        tf = step.flops() / (att_ms * 1e-3) / 1e12
-        roofline_override = {"bound": "tensor", "achieved": tf, "peak": tpk, "unit": "TFLOP/s", "frac": tf / tpk,
-                             "traffic": None, "algorithmic_flops_per_launch": step.flops(),
-                             "kernel": "multi-query attention (chunk queries, causal)",
-                             "avg_launch_us": att_ms * 1e3, "merge_us": (ms - att_ms) * 1e3,
-                             "peak_source": tsrc + (", of measured" if tsrc.startswith("measured")
-                                                    else ", of fallback")}
+        intensity = step.flops() / kv_bytes                    # FLOPs per KV byte read
+        if intensity >= tpk * 1e12 / (peak * 1e9):
+            tf = step.flops() / (att_ms * 1e-3) / 1e12
+            roofline_override = {"bound": "tensor", "achieved": tf, "peak": tpk, "unit": "TFLOP/s",
+                                 "frac": tf / tpk, "algorithmic_flops_per_launch": step.flops(),
+                                 "peak_source": tsrc + (", of measured" if tsrc.startswith("measured")
+                                                        else ", of fallback")}
+        else:
+            roofline_override = {"bound": "hbm", "achieved": att_gbs, "peak": peak, "unit": "GB/s",
+                                 "frac": att_gbs / peak, "algorithmic_bytes_per_launch": kv_bytes,
+                                 "peak_source": peak_src + (", of measured" if peak_src.startswith("measured")
+                                                            else ", of fallback")}
+        roofline_override.update({"traffic": None, "kernel": "multi-query attention (chunk queries, causal)",
+                                  "flops_per_kv_byte": intensity, "avg_launch_us": att_ms * 1e3,
+                                  "merge_us": (ms - att_ms) * 1e3})
     else:
         roofline_override = None
     per_launch_kv = kv_bytes / n_att

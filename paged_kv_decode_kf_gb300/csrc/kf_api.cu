@@ -195,8 +195,11 @@ int decode_impl() {
 
 // Multi-query kernel choice: 0 = mma.sync (32/64-column tiles), 1 = tcgen05
 // with one 128-row query tile and 64-token KV tiles, 2 = tcgen05 with two
-// query tiles and 128-token KV tiles. The 128-row tile pays off from 64 (query,
-// head) rows per KV head; two tiles once a request has more than 128.
+// query tiles and 128-token KV tiles. Two tiles once a request has more than
+// 128 (query, head) rows per KV head, else one: even 8-32 rows (speculative
+// verify of 2-8 tokens at G = 4, HBM-bound) stream KV faster through the
+// one-tile tcgen05 kernel (5.1 TB/s on 64 requests of ~3.8K tokens) than
+// through the mma.sync kernel (4.2 TB/s), the padded rows notwithstanding.
 // KF_MQ_IMPL = "mma", "tc05" or "tc05w" forces one (read per call, so a process
 // can compare them; "tc05w" needs more than 128 rows).
 int multiquery_kernel(int max_query_len, int group) {
@@ -205,7 +208,7 @@ int multiquery_kernel(int max_query_len, int group) {
     if (s && strcmp(s, "mma") == 0) return 0;
     if (s && strcmp(s, "tc05") == 0) return 1;
     if (s && strcmp(s, "tc05w") == 0) return rows > 128 ? 2 : 1;
-    return rows > 128 ? 2 : (rows >= 64 ? 1 : 0);
+    return rows > 128 ? 2 : 1;
 }
 
 }  // namespace kf

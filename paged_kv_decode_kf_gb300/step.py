@@ -136,12 +136,12 @@ class CascadeStep:
         self.max_suffix = int(inp.suffix_ctx_after.max().item())
         # prefix pass: one wave of CTAs (KV heads x query tiles x splits) for the
         # kernel the library picks for B x G rows per KV head: 256 rows and one
-        # CTA per SM (tcgen05, two tiles), 128 rows and two per SM (tcgen05, one
-        # tile), 64 columns and about four per SM (mma.sync)
+        # CTA per SM (tcgen05, two tiles), else 128 rows and two per SM (tcgen05,
+        # one tile)
         if prefix_splits is None:
             sms = torch.cuda.get_device_properties(dev).multi_processor_count
             rows = B * w.group
-            rows_per_cta, per_sm = (256, 1) if rows > 128 else ((128, 2) if rows >= 64 else (64, 4))
+            rows_per_cta, per_sm = (256, 1) if rows > 128 else (128, 2)
             units = w.num_kv_heads * max(1, -(-rows // rows_per_cta))
             prefix_splits = max(1, min(self.P // w.block_size, -(-per_sm * sms // units)))
         if suffix_splits is None:

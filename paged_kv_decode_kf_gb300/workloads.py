@@ -175,6 +175,12 @@ CONFIGS["cascade"] = Workload(
 # Chunked prefill (multi-query, causal): each request's newest `chunk` tokens are
 # in the cache and their queries attend to the paged history and causally to
 # the chunk, not one of the five configs.
+CONFIGS["specverify"] = Workload(
+    name="specverify", batch=64, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+    lengths=Uniform(3584, 4096), seed=1007, chunk=4,
+    description="speculative verify: the llama8b batch (64 requests, U[3.5K,4K] cached tokens, "
+                "32/8 heads, D 128, bs 16) checking 4 draft tokens each, causally")
+
 CONFIGS["chunk"] = Workload(
     name="chunk", batch=4, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
     lengths=Uniform(4096, 12288), seed=1006, chunk=1024,

@@ -189,3 +189,28 @@ def test_chunk_full_size_sampled(kf):
         ref_o, ref_l = oracle.attention(q, hv.k, hv.v, bt, lim, w.scale)
         check_out(step.out[rows].cpu().numpy(), ref_o, "chunk out, request %d" % b)
         check_lse(step.lse[rows].cpu().numpy(), ref_l, "chunk lse, request %d" % b)
+
+
+def test_specverify_full_size_sampled(kf):
+    """The speculative-verify workload at full size (64 requests of U[3.5K,4K]
+    cached tokens, 4 draft queries each, causal: 16 rows per KV head, the
+    one-tile tcgen05 kernel) in the configuration the benchmark times; every
+    draft query of sampled requests against the oracle over its own limit."""
+    from paged_kv_decode_kf_gb300.step import ChunkStep
+    w = wl.CONFIGS["specverify"]
+    dev = wl.make_inputs(w, "cuda")
+    step = ChunkStep(dev)
+    step.run()
+    torch.cuda.synchronize()
+    C = w.chunk
+    reqs = [0, 17, w.batch - 1]
+    hv = HostView(dev, reqs)
+    for idx, b in enumerate(reqs):
+        L = int(hv.ctx_after[idx])
+        rows = [b * C + j for j in range(C)]
+        q = wl.bf16_bits(dev.q_chunk[rows])
+        bt = np.repeat(hv.tables[0][idx:idx + 1], C, axis=0)
+        lim = np.array([L - C + j + 1 for j in range(C)], np.int32)
+        ref_o, ref_l = oracle.attention(q, hv.k, hv.v, bt, lim, w.scale)
+        check_out(step.out[rows].cpu().numpy(), ref_o, "specverify out, request %d" % b)
+        check_lse(step.lse[rows].cpu().numpy(), ref_l, "specverify lse, request %d" % b)
