@@ -89,3 +89,19 @@ def test_chunk_inputs():
     assert torch.equal(plain.k_cache, i.k_cache) and torch.equal(plain.q, i.q)
     lay = wl.plan_layout(wl.CONFIGS["chunk"])
     assert int(lay.ctx_after.min()) >= wl.CONFIGS["chunk"].chunk
+
+
+def test_specverify_inputs():
+    """Speculative verify: the llama8b batch (same heads, dims, block size and
+    length range) with 4 causal draft queries per request, row starts at
+    multiples of 4."""
+    w = wl.CONFIGS["specverify"]
+    base = wl.CONFIGS["llama8b"]
+    assert (w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size) == \
+        (base.batch, base.num_q_heads, base.num_kv_heads, base.head_dim, base.block_size)
+    assert w.chunk == 4 and (w.lengths.lo, w.lengths.hi) == (base.lengths.lo, base.lengths.hi)
+    small = wl.scaled(w, batch=3, lengths=wl.Fixed((10, 3000, 4)))
+    i = wl.make_inputs(small, "cpu")
+    assert tuple(i.q_chunk.shape) == (3 * 4, w.num_q_heads, w.head_dim)
+    assert i.q_start.tolist() == [0, 4, 8, 12]
+    assert int(i.ctx_after.min()) >= w.chunk
