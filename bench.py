@@ -3,7 +3,8 @@
 attention, LSE merge, through the C-ABI library.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload llama8b|longctx|shard4|ragged|tiny]
+                    [--workload llama8b|longctx|shard4|ragged|tiny|cascade|chunk|specverify]
+                    [--kv-dtype bf16|fp8] [--num-splits S]
 
 Prints one JSON line. `value` is KV-read GB/s over all ranks: algorithmic KV
 bytes (sum_b L_b * 2 * Hkv * D * 2) per step divided by the device time of a
@@ -639,7 +640,8 @@ def run_ours(args):
                                                             else ", of fallback")}
         roofline_override.update({"traffic": None, "kernel": "multi-query attention (chunk queries, causal)",
                                   "flops_per_kv_byte": intensity, "avg_launch_us": att_ms * 1e3,
-                                  "merge_us": (ms - att_ms) * 1e3})
+                                  # no merge launch with one split and fp32 output
+                                  "merge_us": (ms - att_ms) * 1e3 if step.merges else 0.0})
     else:
         roofline_override = None
     per_launch_kv = kv_bytes / n_att

@@ -337,6 +337,12 @@ mq5_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
         const uint32_t col_s = Sh::col_s(tq), col_p = Sh::col_p(tq), col_o = Sh::col_o(tq);
         float m = -INFINITY, l = 0.f;
         bool ok = true;
+        // A warp with no row of the request (a short tile: speculative verify
+        // fills 16 of 128 rows) keeps the barrier protocol and its share of the
+        // V-tail zeroing but reads no scores and writes no weights: its P lanes
+        // hold whatever TMEM held, which reaches only its own rows of O (an MMA
+        // row depends on its own row of A alone), and those rows are never stored.
+        const bool live = __any_sync(0xffffffffu, row_ok);
         if (tq < nqt) {
             for (int j = 0; j < ntiles; ++j) {
                 const int64_t t0 = t_lo + (int64_t)j * kTile;
@@ -345,10 +351,12 @@ mq5_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
                     ok = false;
                     break;
                 }
-                tc05::fence_after_sync();
                 uint32_t sr[kTile];
-                tc05::tmem_ld64(tm + lane_base + col_s, sr);
-                tc05::fence_before_sync();
+                if (live) {
+                    tc05::fence_after_sync();
+                    tc05::tmem_ld64(tm + lane_base + col_s, sr);
+                    tc05::fence_before_sync();
+                }
                 mbar_arrive(s_free(tq));
 
                 const int64_t ntile_tok = t_hi - t0 < kTile ? t_hi - t0 : kTile;
@@ -372,13 +380,19 @@ mq5_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
                     }
                     fence_proxy_async_smem();
                 }
+                if (!live) {
+                    mbar_arrive(p_full(tq, j & 1));
+                    continue;
+                }
                 const int64_t nv64 = row_hi - t0;
                 const int nv = nv64 <= 0 ? 0 : (nv64 >= kTile ? kTile : (int)nv64);
                 // Fast path -- every row of the warp sees the whole tile and the
                 // scale is positive: the max of the raw scores (times c), and one
                 // fused multiply-add per weight below. Otherwise scores are scaled
-                // and masked to -inf first.
-                const bool fast = c > 0.f && __all_sync(0xffffffffu, nv == kTile);
+                // and masked to -inf first. Rows past the request (zero q, so
+                // zero scores against the tile's in-context keys) do not force
+                // the masked path.
+                const bool fast = c > 0.f && __all_sync(0xffffffffu, nv == kTile || !row_ok);
                 float mx = -INFINITY;
                 if (fast) {
 #pragma unroll
@@ -448,7 +462,9 @@ mq5_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
             // with the last two PVs still pending, and two phases back has the
             // parity it waits for. (Every other wait here is at most one phase
             // behind its barrier.)
-            if (ok && warp_wait(fin, 0)) {
+            if (ok && !live) {
+                // nothing to store; the issuer waits for the last MMA before TMEM is freed
+            } else if (ok && warp_wait(fin, 0)) {
                 tc05::fence_after_sync();
                 const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
