@@ -176,10 +176,17 @@ def whole_job_gbs(bytes_per_rank: int, world: int, seconds_max: float) -> float:
 # profile-derived DRAM traffic of the attention kernel (null if stale)
 # ----------------------------------------------------------------------------
 
-def kernel_source_digest() -> str:
+# the sources each DRAM-traffic record was captured from
+DIGEST_SOURCES = {
+    "decode": ("kf_decode_tc.cuh", "kf_decode_tc.cu", "kf_internal.cuh"),
+    "mq5": ("kf_multiquery_tc05.cu", "kf_mq_tc05.cuh", "kf_tc05.cuh", "kf_decode_tc.cuh", "kf_internal.cuh"),
+}
+
+
+def kernel_source_digest(which: str = "decode") -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in ("kf_decode_tc.cuh", "kf_decode_tc.cu", "kf_internal.cuh"):
+    for f in DIGEST_SOURCES[which]:
         with open(os.path.join(ROOT, "paged_kv_decode_kf_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -202,6 +209,24 @@ def profiled_traffic(workload: str, kernel: str, kv_bytes_per_launch: float, kv_
         if per is None:
             return None
         # scaled to one launch of this run by the KV bytes it processes
+        return per["dram_bytes_per_launch"] * kv_bytes_per_launch / per["kv_bytes_per_launch"]
+    except Exception:
+        return None
+
+
+def profiled_mq_traffic(workload: str, kv_bytes_per_launch: float):
+    """DRAM traffic of one launch of the one-tile tcgen05 multi-query kernel
+    (query rows per KV head <= 128), scaled to this launch by its KV bytes;
+    None without a record for `workload` taken from the current sources."""
+    path = os.path.join(ROOT, "profiles", "multiquery_dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        if rec.get("kernel_source_digest") != kernel_source_digest("mq5"):
+            return None
+        per = rec.get("per_workload", {}).get(workload)
+        if per is None:
+            return None
         return per["dram_bytes_per_launch"] * kv_bytes_per_launch / per["kv_bytes_per_launch"]
     except Exception:
         return None
@@ -638,7 +663,8 @@ def run_ours(args):
                                  "frac": att_gbs / peak, "algorithmic_bytes_per_launch": kv_bytes,
                                  "peak_source": peak_src + (", of measured" if peak_src.startswith("measured")
                                                             else ", of fallback")}
-        roofline_override.update({"traffic": None, "kernel": "multi-query attention (chunk queries, causal)",
+        roofline_override.update({"traffic": profiled_mq_traffic(w.name, kv_bytes),
+                                  "kernel": "multi-query attention (chunk queries, causal)",
                                   "flops_per_kv_byte": intensity, "avg_launch_us": att_ms * 1e3,
                                   # no merge launch with one split and fp32 output
                                   "merge_us": (ms - att_ms) * 1e3 if step.merges else 0.0})
