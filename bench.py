@@ -180,6 +180,7 @@ def whole_job_gbs(bytes_per_rank: int, world: int, seconds_max: float) -> float:
 DIGEST_SOURCES = {
     "decode": ("kf_decode_tc.cuh", "kf_decode_tc.cu", "kf_internal.cuh"),
     "mq5": ("kf_multiquery_tc05.cu", "kf_mq_tc05.cuh", "kf_tc05.cuh", "kf_decode_tc.cuh", "kf_internal.cuh"),
+    "mqw": ("kf_multiquery_tc05w.cu", "kf_mq_tc05.cuh", "kf_tc05.cuh", "kf_decode_tc.cuh", "kf_internal.cuh"),
 }
 
 
@@ -214,15 +215,17 @@ def profiled_traffic(workload: str, kernel: str, kv_bytes_per_launch: float, kv_
         return None
 
 
-def profiled_mq_traffic(workload: str, kv_bytes_per_launch: float):
-    """DRAM traffic of one launch of the one-tile tcgen05 multi-query kernel
-    (query rows per KV head <= 128), scaled to this launch by its KV bytes;
-    None without a record for `workload` taken from the current sources."""
+def profiled_mq_traffic(workload: str, rows_per_kv_head: int, kv_bytes_per_launch: float):
+    """DRAM traffic of one launch of the tcgen05 multi-query kernel the library
+    picks for this many query rows per KV head (the one-tile kernel up to 128,
+    the wide one above), scaled to this launch by its KV bytes; None without a
+    record for `workload` taken from the current sources of that kernel."""
     path = os.path.join(ROOT, "profiles", "multiquery_dram_traffic.json")
+    kernel = "mq5" if rows_per_kv_head <= 128 else "mqw"
     try:
         with open(path) as f:
-            rec = json.load(f)
-        if rec.get("kernel_source_digest") != kernel_source_digest("mq5"):
+            rec = json.load(f)["kernels"][kernel]
+        if rec.get("kernel_source_digest") != kernel_source_digest(kernel):
             return None
         per = rec.get("per_workload", {}).get(workload)
         if per is None:
@@ -663,7 +666,7 @@ def run_ours(args):
                                  "frac": att_gbs / peak, "algorithmic_bytes_per_launch": kv_bytes,
                                  "peak_source": peak_src + (", of measured" if peak_src.startswith("measured")
                                                             else ", of fallback")}
-        roofline_override.update({"traffic": profiled_mq_traffic(w.name, kv_bytes),
+        roofline_override.update({"traffic": profiled_mq_traffic(w.name, step.C * w.group, kv_bytes),
                                   "kernel": "multi-query attention (chunk queries, causal)",
                                   "flops_per_kv_byte": intensity, "avg_launch_us": att_ms * 1e3,
                                   # no merge launch with one split and fp32 output
