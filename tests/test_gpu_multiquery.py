@@ -214,3 +214,37 @@ def test_specverify_full_size_sampled(kf):
         ref_o, ref_l = oracle.attention(q, hv.k, hv.v, bt, lim, w.scale)
         check_out(step.out[rows].cpu().numpy(), ref_o, "specverify out, request %d" % b)
         check_lse(step.lse[rows].cpu().numpy(), ref_l, "specverify lse, request %d" % b)
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+@pytest.mark.parametrize("causal", [True, False])
+def test_multiquery_nonfinite_garbage_past_context(kf, impl, causal):
+    """Slots past each request's end (same blocks) and unused blocks hold
+    NaN/Inf: results must be unaffected -- with query tiles whose warps hold
+    no row (4 tokens x G 4 = 16 of 128 rows), partly filled warps (12 and 44
+    rows) and full ones."""
+    lengths, chunks = (300, 1000, 77, 4096, 45, 130), (4, 4, 3, 4, 11, 32)
+    w, dev, q, qs = _case(lengths, chunks, seed=11)
+    bt = dev.block_tables.cpu().numpy()
+    L = dev.ctx_after.cpu().numpy()
+    used = set()
+    for b in range(w.batch):
+        n = -(-int(L[b]) // w.block_size)
+        used |= set(bt[b, :n].tolist())
+        last = bt[b, n - 1]
+        for t in range(int(L[b]) % w.block_size or w.block_size, w.block_size):
+            dev.k_cache[last, t] = float("nan")
+            dev.v_cache[last, t] = float("inf") if t % 2 else float("nan")
+    for p in range(dev.num_blocks):
+        if p not in used:
+            dev.k_cache[p] = float("nan")
+            dev.v_cache[p] = float("nan")
+    hq_, qs_h, k, v, bt_h, ctx = _host(dev, q, qs)
+    maxL, maxC = int(max(lengths)), int(max(chunks))
+    for S in (1, 3):
+        with mq_impl(impl):
+            o_p, l_p = kf.kf_paged_multiquery_attention(q, qs, dev.k_cache, dev.v_cache, dev.block_tables,
+                                                        dev.ctx_after, causal, maxL, maxC, w.scale, S)
+        ref_po, ref_pl = oracle.multiquery_partials(hq_, qs_h, k, v, bt_h, ctx, w.scale, causal, S,
+                                                    max_context_len=maxL)
+        check_partials(o_p.cpu().numpy(), l_p.cpu().numpy(), ref_po, ref_pl, "garbage partials")
