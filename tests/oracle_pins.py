@@ -278,6 +278,13 @@ def pin_merge_properties(lib):
     # weights e^{lse_i}: closed form against direct normalised weights
     wts = np.exp(lse - lse.max())
     np.testing.assert_allclose(full, (wts[:, None] * o).sum(0) / wts.sum(), rtol=0, atol=1e-13)
+    # an empty partial first and one partial 895 above another: the weights
+    # are e^{lse_i - max}, so the result is the top partial exactly (e^-895
+    # is 0 in double); a shift by any lse but the maximum yields -inf here or
+    # overflows
+    top, ltop = oracle.merge(np.stack([np.zeros(6), o[0], o[1]]), np.array([-math.inf, 5.0, 900.0]), lib=lib)
+    np.testing.assert_array_equal(top, o[1])
+    assert ltop == 900.0
 
 
 def pin_shift_invariance(lib):

@@ -40,6 +40,14 @@ MUTANTS = {
     "fp8_k_scale_is_v_scale": ("(double)k_scale[kvh],", "(double)v_scale[kvh],"),
     "chunk_causal_off_by_one": ("int64_t limit = causal ? L - C + j + 1 : L;", "int64_t limit = causal ? L - C + j : L;"),
     "chunk_causal_reversed": ("int64_t limit = causal ? L - C + j + 1 : L;", "int64_t limit = causal ? L - j : L;"),
+    "chunk_split_not_clipped": ("                    if (t1 > limit)\n                        t1 = limit;",
+                                "                    (void)limit;"),
+    "chunk_kv_head_interleaved": ("num_kv_heads, head_dim, h / G, t0, t1, scale,",
+                                  "num_kv_heads, head_dim, h % num_kv_heads, t0, t1, scale,"),
+    "chunk_ignores_q_start": ("int64_t n = q_start[b] + j;", "int64_t n = j;"),
+    "chunk_limit_from_max_context": ("int64_t limit = causal ? L - C + j + 1 : L;",
+                                     "int64_t limit = causal ? max_context_len - C + j + 1 : L;"),
+    "merge_max_is_first": ("        if (li > M)\n            M = li;", "        if (i == 0)\n            M = li;"),
     "fp8_append_multiplies": ("float kq = (float)kfo_bf16_to_double(k_new[src + d]) / k_scale[h];",
                               "float kq = (float)kfo_bf16_to_double(k_new[src + d]) * k_scale[h];"),
 }
