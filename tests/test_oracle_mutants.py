@@ -48,6 +48,10 @@ MUTANTS = {
     "chunk_limit_from_max_context": ("int64_t limit = causal ? L - C + j + 1 : L;",
                                      "int64_t limit = causal ? max_context_len - C + j + 1 : L;"),
     "merge_max_is_first": ("        if (li > M)\n            M = li;", "        if (i == 0)\n            M = li;"),
+    "split_chunk_floor": ("int64_t chunk = (n_max + num_splits - 1) / num_splits;",
+                          "int64_t chunk = n_max / num_splits;"),
+    "e4m3_subnormal_scale": ("v = ldexp((double)m, -9);", "v = ldexp((double)m, -10);"),
+    "e4m3_nan_code_ignored": ("    if (e == 15 && m == 7)\n        return NAN;", "    if (e == 15 && m == 7 && sign)\n        return NAN;"),
     "fp8_append_multiplies": ("float kq = (float)kfo_bf16_to_double(k_new[src + d]) / k_scale[h];",
                               "float kq = (float)kfo_bf16_to_double(k_new[src + d]) * k_scale[h];"),
 }
