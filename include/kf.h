@@ -124,7 +124,11 @@ kf_status kf_append_kv(const void *k_new, const void *v_new, void *k_cache, void
  *                    0 is allowed (every split empty)
  *   max_context_len  host-side upper bound of context_lens (sets the chunk c)
  *   scale            softmax scale, e.g. 1/sqrt(head_dim)
- *   num_splits       >= 1; see kf_choose_num_splits
+ *   num_splits       >= 1; see kf_choose_num_splits. 0 is not "let the library
+ *                    choose" here: the caller sizes out_partial and lse_partial,
+ *                    so it fixes num_splits (kf_choose_num_splits gives the
+ *                    library's plan; the step calls, whose partials are
+ *                    internal, take 0 as their own schedule)
  *
  * A shard (a token-range partition held under its own block table, as on
  * KernelFlume's attention nodes) is one call with that shard's table and
@@ -198,6 +202,9 @@ kf_status kf_paged_multiquery_attention(const void *q, const int32_t *q_start, c
  * context_lens_host (int32 [batch], host memory, nullable) is given it plans
  * for those lengths; otherwise it assumes every request has max_context_len
  * tokens. Returns a value < 1 on invalid arguments or a CUDA error.
+ * The plan needs the head counts and head_dim (they fix the kernel's work
+ * units and bytes per token) and, when given, every request's length (a
+ * ragged batch plans differently from one of max_context_len throughout).
  */
 int kf_choose_num_splits(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                          int block_size, int max_context_len, const int32_t *context_lens_host,
@@ -408,14 +415,18 @@ kf_status kf_decode_step_fp8(const void *q, const void *k_new, const void *v_new
  *  - Calls whose kf_decode_step_workspace_size(...) exceeds
  *    KF_STATIC_SCRATCH_BYTES return KF_ERR_UNSUPPORTED (use kf_decode_step with
  *    your own workspace, or fewer splits).
+ *  - Shapes the step does not support, bad arguments and a device that cannot
+ *    be queried give the same status as kf_decode_step with a workspace.
  *  - The first call on a device looks up the array's device address (a
- *    one-time set-up on that device); make that first call before any stream
- *    capture.
+ *    one-time set-up on that device, repeated in a new context of the device,
+ *    e.g. after cudaDeviceReset, because the array may then sit elsewhere);
+ *    make that first call before any stream capture.
  *  - Every call on a device shares the one array, which keeps the previous
  *    call's contents; each call clears the part that must start at zero (the
- *    merge counters) on its own stream. Calls that overlap on the GPU (on
- *    different streams, or from different threads) race on the array and
- *    give wrong results: serialise them.
+ *    merge counters) on its own stream, after every argument check, so a
+ *    refused call queues no work. Calls that overlap on the GPU (on different
+ *    streams, or from different threads) race on the array and give wrong
+ *    results: serialise them.
  */
 #define KF_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
@@ -432,6 +443,8 @@ kf_status kf_decode_step_static(const void *q, const void *k_new, const void *v_
  * Synchronises `stream`, copies the word (KF_DEVERR_* bits) to *flags and
  * resets it to 0. Returns KF_OK if no bit was set, KF_ERR_DEVICE if some
  * bit was, KF_ERR_CUDA if a CUDA call failed, KF_ERR_INVALID if flags is NULL.
+ * One status covers every kind of device error (a bad block id, a length out
+ * of range, a wait that gave up); the bits in *flags say which occurred.
  */
 kf_status kf_get_device_error(unsigned int *flags, kf_stream_t stream);
 

@@ -23,12 +23,38 @@ namespace kf {
 // address with cudaGetSymbolAddress, once per device.
 static __device__ unsigned int g_error_word;
 
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     bool ready = false;
+    unsigned long long ctx_id = 0;  // context the facts below were taken in
     int sm_count = 0;
     unsigned int *err = nullptr;
 };
@@ -38,7 +64,8 @@ DeviceInfo g_devices[kMaxDevices];
 void *g_encode_fn = nullptr;
 bool g_encode_tried = false;
 
-// Per-device facts, set up on first use with that device current.
+// Per-device facts, set up on first use with that device current (and again
+// in a new context of that device).
 cudaError_t device_info(DeviceInfo **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -46,11 +73,15 @@ cudaError_t device_info(DeviceInfo **out) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceInfo &d = g_devices[dev];
-    if (!d.ready) {
+    // a context torn down and created again (cudaDeviceReset) reloads the
+    // module, so the address is looked up again in a new context
+    if (!d.ready || d.ctx_id != current_context_id()) {
+        d.ready = false;
         e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         e = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_error_word);
         if (e != cudaSuccess) return e;
+        d.ctx_id = current_context_id();
         d.ready = true;
     }
     *out = &d;
@@ -484,7 +515,7 @@ kf_status bal_step(const void *q, const void *k_new, const void *v_new, void *k_
                    int block_size, int64_t num_blocks, float scale, void *workspace,
                    size_t workspace_bytes, void *out, kf_dtype out_dtype, float *lse_out,
                    const float *k_scale, const float *v_scale, bool kv8, const float *ex_o,
-                   const float *ex_lse, int n_ex, kf_stream_t stream) {
+                   const float *ex_lse, int n_ex, bool clear_counters, kf_stream_t stream) {
     if (!workspace || !aligned16(workspace)) return KF_ERR_INVALID;
     DeviceInfo *dev = nullptr;
     if (device_info(&dev) != cudaSuccess) return KF_ERR_CUDA;
@@ -527,6 +558,9 @@ kf_status bal_step(const void *q, const void *k_new, const void *v_new, void *k_
     void *fn = encode_fn();
     if (!fn) return KF_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_counters &&
+        cudaMemsetAsync(a.counters, 0, (size_t)batch * num_kv_heads * 4, st) != cudaSuccess)
+        return KF_ERR_CUDA;
     const cudaError_t e = kv8 ? launch_decode_step_bal_fp8(p, a, (int)ctas, st, fn)
                               : launch_decode_step_bal(p, a, (int)ctas, st, fn);
     if (e == cudaErrorInvalidValue) return KF_ERR_UNSUPPORTED;
@@ -540,7 +574,7 @@ kf_status step_impl(const void *q, const void *k_new, const void *v_new, void *k
                     int64_t num_blocks, float scale, int num_splits, void *workspace,
                     size_t workspace_bytes, void *out, kf_dtype out_dtype, float *lse_out,
                     const float *k_scale, const float *v_scale, bool kv8, const float *ex_o,
-                    const float *ex_lse, int n_ex, kf_stream_t stream) {
+                    const float *ex_lse, int n_ex, bool clear_counters, kf_stream_t stream) {
     if (batch < 0 || num_splits < 0 || bt_stride < 1 || num_blocks < 1 || max_context_len < 0 ||
         num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || block_size < 1 || !isfinite(scale) ||
         (out_dtype != KF_BF16 && out_dtype != KF_F32) || n_ex < 0)
@@ -560,7 +594,7 @@ kf_status step_impl(const void *q, const void *k_new, const void *v_new, void *k
         return bal_step(q, k_new, v_new, k_cache, v_cache, block_tables, bt_stride, context_lens_before,
                         max_context_len, batch, num_q_heads, num_kv_heads, head_dim, block_size,
                         num_blocks, scale, workspace, workspace_bytes, out, out_dtype, lse_out, k_scale,
-                        v_scale, kv8, ex_o, ex_lse, n_ex, stream);
+                        v_scale, kv8, ex_o, ex_lse, n_ex, clear_counters, stream);
     const size_t need = kf_decode_step_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
                                                       num_splits);
     const bool counted = num_splits > 1 || n_ex > 0;  // some group merges: counters needed
@@ -622,6 +656,9 @@ kf_status step_impl(const void *q, const void *k_new, const void *v_new, void *k
     void *fn = encode_fn();
     if (!fn) return KF_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_counters && a.counters &&
+        cudaMemsetAsync(a.counters, 0, (size_t)batch * num_kv_heads * 4, st) != cudaSuccess)
+        return KF_ERR_CUDA;
     return from_cuda(kv8 ? launch_decode_step_tc_fp8(p, a, st, fn) : launch_decode_step_tc(p, a, st, fn));
 }
 
@@ -641,7 +678,7 @@ kf_status kf_decode_step(const void *q, const void *k_new, const void *v_new, vo
                      context_lens_before, max_context_len, batch, num_q_heads, num_kv_heads,
                      head_dim, block_size, num_blocks, scale, num_splits, workspace,
                      workspace_bytes, out, out_dtype, lse_out, nullptr, nullptr, false, nullptr,
-                     nullptr, 0, stream);
+                     nullptr, 0, false, stream);
 }
 
 kf_status kf_decode_step_merge_partials(const void *q, const void *k_new, const void *v_new,
@@ -658,7 +695,7 @@ kf_status kf_decode_step_merge_partials(const void *q, const void *k_new, const 
                      context_lens_before, max_context_len, batch, num_q_heads, num_kv_heads,
                      head_dim, block_size, num_blocks, scale, num_splits, workspace,
                      workspace_bytes, out, out_dtype, lse_out, nullptr, nullptr, false,
-                     extra_out_partial, extra_lse_partial, num_extra, stream);
+                     extra_out_partial, extra_lse_partial, num_extra, false, stream);
 }
 
 kf_status kf_decode_step_fp8(const void *q, const void *k_new, const void *v_new, void *k_cache,
@@ -673,10 +710,33 @@ kf_status kf_decode_step_fp8(const void *q, const void *k_new, const void *v_new
                      context_lens_before, max_context_len, batch, num_q_heads, num_kv_heads,
                      head_dim, block_size, num_blocks, scale, num_splits, workspace,
                      workspace_bytes, out, out_dtype, lse_out, k_scale, v_scale, true, nullptr,
-                     nullptr, 0, stream);
+                     nullptr, 0, false, stream);
 }
 
 }  // extern "C"
+
+namespace kf {
+
+// kf_decode_step with the workspace's merge counters cleared on the stream
+// after every argument check, right before the launch (the scratch of
+// kf_decode_step_static keeps the previous call's contents).
+kf_status decode_step_clearing_counters(const void *q, const void *k_new, const void *v_new,
+                                        void *k_cache, void *v_cache, const int32_t *block_tables,
+                                        int bt_stride, const int32_t *context_lens_before,
+                                        int max_context_len, int batch, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int64_t num_blocks, float scale, int num_splits,
+                                        void *workspace, size_t workspace_bytes, void *out,
+                                        kf_dtype out_dtype, float *lse_out, kf_stream_t stream) {
+    return step_impl(q, k_new, v_new, k_cache, v_cache, block_tables, bt_stride,
+                     context_lens_before, max_context_len, batch, num_q_heads, num_kv_heads,
+                     head_dim, block_size, num_blocks, scale, num_splits, workspace,
+                     workspace_bytes, out, out_dtype, lse_out, nullptr, nullptr, false, nullptr,
+                     nullptr, 0, true, stream);
+}
+
+}  // namespace kf
+
 
 namespace {
 

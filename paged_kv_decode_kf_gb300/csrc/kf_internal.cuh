@@ -95,6 +95,21 @@ cudaError_t launch_decode_step_bal_fp8(const DecodeParams &p, const StepArgs &a,
                                        cudaStream_t stream, void *encode_fn);
 // One bounded wait that nothing completes (sets KF_DEVERR_TIMEOUT).
 cudaError_t launch_wait_check(unsigned int *err, cudaStream_t stream);
+
+// Process-unique id of the CUDA context current on the calling thread (0 if
+// none): device addresses looked up in one context are stale in the next.
+unsigned long long current_context_id();
+
+// kf_decode_step that clears its workspace's merge counters on `stream` after
+// every argument check, right before the launch.
+kf_status decode_step_clearing_counters(const void *q, const void *k_new, const void *v_new,
+                                        void *k_cache, void *v_cache, const int32_t *block_tables,
+                                        int bt_stride, const int32_t *context_lens_before,
+                                        int max_context_len, int batch, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int64_t num_blocks, float scale, int num_splits,
+                                        void *workspace, size_t workspace_bytes, void *out,
+                                        kf_dtype out_dtype, float *lse_out, kf_stream_t stream);
 // Bytes of the tensor-core kernel's shared-memory ring (the fused merge reuses it).
 int decode_tc_ring_bytes(int num_kv_heads, int head_dim, bool kv8);
 // Largest number of resident CTAs per SM and KV heads per CTA the tensor-core

@@ -12,7 +12,8 @@
 // The array is a file-scope __device__ variable: every GPU on which the
 // library's device code is loaded holds it until the process exits. In host
 // code its name is only a host-side stand-in, so its device address is taken
-// with cudaGetSymbolAddress, once per device, with that device current.
+// with cudaGetSymbolAddress, once per device (and again if that device's
+// context is torn down and created anew), with that device current.
 #include <mutex>
 
 #include "kf_internal.cuh"
@@ -25,23 +26,30 @@ static __device__ __align__(256) unsigned char g_step_scratch[KF_STATIC_SCRATCH_
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-void *g_scratch[kMaxDevices];
+struct ScratchAddress {
+    void *ptr = nullptr;
+    unsigned long long ctx_id = 0;  // the context `ptr` was looked up in
+};
+ScratchAddress g_scratch[kMaxDevices];
 
 // Device address of the scratch array on the current device (set up on the
-// first call for that device).
+// first call for that device, and again in a new context of it: a device
+// reset reloads the module, which may place the array elsewhere).
 cudaError_t scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_scratch[dev] == nullptr) {
+    ScratchAddress &s = g_scratch[dev];
+    if (s.ptr == nullptr || s.ctx_id != current_context_id()) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_step_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch[dev] = p;
+        s.ptr = p;
+        s.ctx_id = current_context_id();
     }
-    *out = g_scratch[dev];
+    *out = s.ptr;
     return cudaSuccess;
 }
 
@@ -58,29 +66,20 @@ extern "C" kf_status kf_decode_step_static(
         return KF_ERR_INVALID;
     if (batch == 0) return KF_OK;
     const bool uses = num_splits != 1;  // the split rule with S > 1, or the balanced schedule
-    const size_t need =
-        kf_decode_step_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, num_splits);
-    if (uses && need == 0) return num_splits == KF_SPLITS_BALANCED ? KF_ERR_CUDA : KF_ERR_INVALID;
-    if (uses && need > (size_t)KF_STATIC_SCRATCH_BYTES) return KF_ERR_UNSUPPORTED;
+    // Scratch beyond the array is refused here; a size of 0 (shapes the step
+    // does not support, or a device that cannot be queried) is left to
+    // kf_decode_step's own checks, so both calls report the same status.
+    if (uses && kf_decode_step_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                              num_splits) > (size_t)KF_STATIC_SCRATCH_BYTES)
+        return KF_ERR_UNSUPPORTED;
     void *scratch = nullptr;
     if (kf::scratch_address(&scratch) != cudaSuccess) return KF_ERR_CUDA;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (uses) {
-        // the merge counters must start at zero; the array keeps whatever the
-        // previous call left, so clear them on this call's stream (split rule:
-        // after the partials; balanced schedule: at the start)
-        size_t ctr_off = 0;
-        if (num_splits > 1) {
-            const size_t rows = (size_t)batch * num_q_heads;
-            const auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-            ctr_off = al((size_t)num_splits * rows * head_dim * 4) + al((size_t)num_splits * rows * 4);
-        }
-        if (cudaMemsetAsync(static_cast<unsigned char *>(scratch) + ctr_off, 0,
-                            (size_t)batch * num_kv_heads * 4, st) != cudaSuccess)
-            return KF_ERR_CUDA;
-    }
-    return kf_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, bt_stride,
-                          context_lens_before, max_context_len, batch, num_q_heads, num_kv_heads,
-                          head_dim, block_size, num_blocks, scale, num_splits, uses ? scratch : nullptr,
-                          uses ? (size_t)KF_STATIC_SCRATCH_BYTES : 0, out, out_dtype, lse_out, stream);
+    // The merge counters must start at zero, and the array keeps whatever the
+    // previous call left: the step clears them on this call's stream once every
+    // argument has passed its checks, so a refused call queues no work.
+    return kf::decode_step_clearing_counters(
+        q, k_new, v_new, k_cache, v_cache, block_tables, bt_stride, context_lens_before,
+        max_context_len, batch, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+        num_splits, uses ? scratch : nullptr, uses ? (size_t)KF_STATIC_SCRATCH_BYTES : 0, out,
+        out_dtype, lse_out, stream);
 }
