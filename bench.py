@@ -3,16 +3,24 @@
 attention, LSE merge, through the C-ABI library.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload llama8b|longctx|shard4|ragged|tiny|cascade|chunk|specverify]
-                    [--kv-dtype bf16|fp8] [--num-splits S]
+                    [--workload ragged|llama8b|longctx|shard4|tiny|cascade|chunk|specverify]
+                    [--kv-dtype bf16|fp8] [--num-splits S] [--out-dtype bf16|f32]
 
-Prints one JSON line. `value` is KV-read GB/s over all ranks: algorithmic KV
-bytes (sum_b L_b * 2 * Hkv * D * 2) per step divided by the device time of a
-step, inputs resident in HBM, timed with CUDA events between a barrier and a
-synchronize on both sides, max over ranks. `e2e` is the same metric with the
-step's inputs copied from pinned host memory and its result copied back
-inside the timed region. `--impl reference` times the fp64 CPU oracle on this
-machine's host cores on a bounded sample of the same workload.
+Prints one JSON line. The default workload is the largest one-GPU
+configuration: the ragged continuous batch (256 requests, 70/25/5 % of them
+1K-8K / 8K-64K / 64K-128K tokens, block size 32) with its append. `value` is
+KV-read GB/s over all ranks: algorithmic KV bytes (sum_b L_b * 2 * Hkv * D *
+2) per step divided by the device time of a step, inputs resident in HBM,
+timed with CUDA events between a barrier and a synchronize on both sides, max
+over ranks. `e2e` is the same metric with the step's inputs copied from pinned
+host memory and its result copied back inside the timed region, with the
+split of its time into copies, device step and host launch/wait.
+`per_config` (one GPU, default workload) times every decode configuration
+(tiny, llama8b, longctx, shard4, ragged): per-step median / p10 / p90 over
+at least 50 graph-replayed steps, KV GB/s and its fraction of the measured
+HBM peak, next to the fp64 oracle timed on the host cores on a bounded
+sample of the same configuration. `--impl reference` times the fp64 CPU
+oracle on this machine's host cores on a bounded sample of the same workload.
 
 With N > 1 (torchrun), every rank runs its own copy of the workload on its own
 GPU (independent batches, no data-path collective: weak scaling).
@@ -43,7 +51,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--workload", default="ragged")
     ap.add_argument("--decode-kernel", default="tc", choices=["tc", "simt"])
     ap.add_argument("--path", default="auto", choices=["auto", "fused", "calls", "cascade", "cascade-calls"],
                     help="fused: kf_decode_step (one launch); calls: append, attention, merge; "
@@ -59,8 +67,12 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="single-launch step: launch each step from the host instead of replaying a "
                          "CUDA graph of consecutive steps")
+    ap.add_argument("--out-dtype", default="bf16", choices=["bf16", "f32"],
+                    help="element type of the step's output rows (the partials and lse stay fp32)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-configuration table (it runs on one GPU, default workload only)")
     return ap.parse_args()
 
 
@@ -97,6 +109,7 @@ def tensor_peak():
 # ----------------------------------------------------------------------------
 
 class ClockSampler:
+    INTERVAL_MS = 50
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -111,7 +124,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -124,7 +137,10 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append((time.time(), line.strip()))
 
-    def stop(self, t0: float, t1: float):
+    def stop(self, t0: float, t1: float, more_windows=()):
+        """Clocks over the timed region [t0, t1]; `more_windows` are further
+        timed regions of the same run (the per-configuration loops), counted in
+        when the main region is too short for three samples."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         time.sleep(0.25)
@@ -142,12 +158,23 @@ class ClockSampler:
                 rows.append((ts, float(parts[0]), float(parts[1]), parts[3:7]))
             except ValueError:
                 continue
-        inside = [r for r in rows if t0 - 0.15 <= r[0] <= t1 + 0.15] or rows[-3:]
+        def within(a, b):
+            return [r for r in rows if a - 0.03 <= r[0] <= b + 0.03]
+        main = within(t0, t1)
+        window = "timed region"
+        inside = main
+        if len(main) < 3 and more_windows:
+            inside = main + [r for a, b in more_windows for r in within(a, b)]
+            window = "timed region + the per-configuration timed loops (the timed region alone is %.0f ms)" % (
+                (t1 - t0) * 1e3)
+        if not inside:
+            inside, window = rows[-3:], "last samples (no sample fell inside a timed region)"
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
                 "sm_max_mhz": max([r[2] for r in inside]) if inside else None,
-                "reasons": reasons, "samples": len(inside)}
+                "reasons": reasons, "samples": len(inside), "samples_in_timed_region": len(main),
+                "interval_ms": self.INTERVAL_MS, "window": window}
 
 
 # ----------------------------------------------------------------------------
@@ -227,6 +254,35 @@ def l2_note(kv_bytes: float, dev) -> str:
         return ("no flush: the %.0f MB of inputs a step reads (KV %.0f MB + queries %.0f MB) exceed the 129 MB L2"
                 % ((kv_bytes + q_bytes) / 1e6, kv_bytes / 1e6, q_bytes / 1e6))
     return "inputs fit in L2 (launch-bound case)"
+
+
+def workload_config(w) -> dict:
+    """The `config` object of both arms' JSON lines: the workload and its
+    sizes, from the seeded layout alone (so the GPU line and the oracle's
+    line carry the same object for the same workload)."""
+    from paged_kv_decode_kf_gb300 import workloads as wl
+    lay = wl.plan_layout(w)
+    kvpt = w.kv_bytes_per_token()
+    logical = int(lay.ctx_after.astype("int64").sum()) * kvpt
+    if w.shared_prefix:     # the prefix once, each request's suffix once
+        read = (int(w.shared_prefix) + int((lay.suffix_ctx_before + 1).sum())) * kvpt
+    else:
+        read = logical
+    elt = 2
+    q_bytes = w.batch * w.num_q_heads * w.head_dim * elt + 2 * w.batch * w.num_kv_heads * w.head_dim * elt
+    if w.chunk:
+        q_bytes += w.batch * w.chunk * w.num_q_heads * w.head_dim * elt
+    if read > L2_BYTES:
+        l2 = "no flush: the %.2f GB of KV read per step exceeds the 129 MB L2" % (read / 1e9)
+    elif read + q_bytes > L2_BYTES:
+        l2 = ("no flush: the %.0f MB of inputs a step reads (KV %.0f MB + queries %.0f MB) exceed the 129 MB L2"
+              % ((read + q_bytes) / 1e6, read / 1e6, q_bytes / 1e6))
+    else:
+        l2 = "inputs fit in L2 (launch-bound case)"
+    return {"workload": w.name + ": " + w.description, "batch": w.batch, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+            "kv_dtype": w.kv_dtype, "kv_bytes_per_step": read, "logical_kv_bytes_per_step": logical,
+            "l2": l2}
 
 
 def profiled_mq_traffic(workload: str, rows_per_kv_head: int, kv_bytes_per_launch: float):
@@ -364,8 +420,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": K, "warmup": W, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name + ": " + w.description, "sample_requests": sample.batch,
-                   "sample_kv_bytes": kv},
+        "config": workload_config(w),
+        "run": {"sample_requests": sample.batch, "sample_kv_bytes": kv,
+                "path": "fp64 C oracle: append, then attention over every query head, threaded over rows"},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": "%d of %d requests of %s per step (%.3f GB of KV)"
                                    % (sample.batch, w.batch, w.name, kv / 1e9)},
@@ -375,8 +432,193 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------
+# every decode configuration in one run
+# ----------------------------------------------------------------------------
+
+PER_CONFIG = ("tiny", "llama8b", "longctx", "shard4", "ragged")
+
+
+def percentile(xs, q: float) -> float:
+    """Linear-interpolated percentile q in [0, 100] of a non-empty list."""
+    ys = sorted(xs)
+    pos = (len(ys) - 1) * q / 100.0
+    lo = int(math.floor(pos))
+    hi = min(lo + 1, len(ys) - 1)
+    return ys[lo] + (ys[hi] - ys[lo]) * (pos - lo)
+
+
+def step_distribution(step, min_samples: int = 50, target_s: float = 0.25):
+    """Per-step device times (ms) of `step` replayed from CUDA graphs.
+
+    A sample is one graph replay of g consecutive steps divided by g, with g
+    the smallest count that makes a sample at least 200 us (g = 1 for every
+    step that long on its own, so most samples are single steps). The stream
+    first sleeps while the host enqueues every replay and event, so the events
+    see device time, not host launch gaps. Returns (samples, g, the wall-clock
+    window of the loop)."""
+    import torch
+    for _ in range(5):
+        step.run()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(10):
+        step.run()
+    b.record()
+    torch.cuda.synchronize()
+    est_ms = max(a.elapsed_time(b) / 10, 1e-3)
+    g = max(1, int(math.ceil(0.2 / est_ms)))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(g):
+            step.run()
+    graph.replay()
+    torch.cuda.synchronize()
+    n = int(min(2000, max(min_samples, math.ceil(target_s * 1e3 / (g * est_ms)))))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    t0 = time.time()
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(40_000_000)        # ~20 ms at 2 GHz: the host enqueues ahead
+    ev[0].record()
+    for i in range(n):
+        graph.replay()
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    samples = [ev[i].elapsed_time(ev[i + 1]) / g for i in range(n)]
+    del graph
+    return samples, g, (t0, t1)
+
+
+def step_phases(step, n: int = 20):
+    """Device time of each launch of a multi-launch step (append, attention
+    per view, merge), from host-launched steps enqueued behind a stream sleep;
+    None for the one-launch step."""
+    import torch
+    if step.fused:
+        return None
+    nv = len(step.views)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nv + 3)] for _ in range(n)]
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(40_000_000)
+    from paged_kv_decode_kf_gb300 import kf
+    i_ = step.inp
+    for e in evs:
+        e[0].record()
+        if step.with_append:
+            step.append()
+        e[1].record()
+        S = step.num_splits
+        for j, (bt, ctx, max_ctx) in enumerate(step.views):
+            # one attention launch per token-range view, as DecodeStep.attention
+            if step.fp8:
+                kf.kf_paged_decode_attention_fp8(i_.q, i_.k_cache, i_.v_cache, i_.k_scale, i_.v_scale, bt, ctx,
+                                                 max_ctx, step.w.scale, S, step.out_partial[j * S:(j + 1) * S],
+                                                 step.lse_partial[j * S:(j + 1) * S])
+            else:
+                kf.kf_paged_decode_attention(i_.q, i_.k_cache, i_.v_cache, bt, ctx, max_ctx, step.w.scale, S,
+                                             step.out_partial[j * S:(j + 1) * S],
+                                             step.lse_partial[j * S:(j + 1) * S])
+            e[2 + j].record()
+        step.merge()
+        e[nv + 2].record()
+    torch.cuda.synchronize()
+    med = lambda k: statistics.median(e[k].elapsed_time(e[k + 1]) for e in evs) * 1e3
+    out = {"append_us": med(0)}
+    for j in range(nv):
+        out["attention_%d_us" % j] = med(1 + j)
+    out["merge_us"] = med(nv + 1)
+    return out
+
+
+def per_config_table(device: str, out_dtype, reuse: dict, peak: float, oracle_s: float = 3.0):
+    """Every decode configuration on this GPU: per-step distribution, KV GB/s
+    and its fraction of `peak`, the per-launch split of multi-launch steps,
+    and the fp64 oracle on the host cores on a bounded sample of the same
+    configuration. `reuse` maps a configuration name to inputs already on the
+    device. Returns (table, timed windows)."""
+    import torch
+    from paged_kv_decode_kf_gb300 import workloads as wl
+    from paged_kv_decode_kf_gb300.step import DecodeStep
+    table, windows = {}, []
+    for name in PER_CONFIG:
+        w = wl.CONFIGS[name]
+        dev = reuse.get(name) or wl.make_inputs(w, device)
+        step = DecodeStep(dev, fused=not w.shards, out_dtype=out_dtype)
+        samples, g, win = step_distribution(step)
+        windows.append(win)
+        phases = step_phases(step)
+        from paged_kv_decode_kf_gb300 import kf
+        flags = kf.kf_get_device_error()
+        if flags:
+            raise RuntimeError("device error word 0x%x after the %s loop" % (flags, name))
+        kv = float(dev.kv_bytes())
+        med = statistics.median(samples)
+        gbs = kv / (med * 1e-3) / 1e9
+        cpu = cpu_baseline(w, target_s=oracle_s)
+        table[name] = {
+            "workload": w.description, "batch": w.batch, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+            "num_splits": step.num_splits, "kv_bytes_per_step": int(kv),
+            "path": ("kf_decode_step (one launch)" if step.fused else
+                     "kf_append_kv + kf_paged_decode_attention x%d + kf_merge_partials" % len(step.views)),
+            "us_median": med * 1e3, "us_p10": percentile(samples, 10) * 1e3,
+            "us_p90": percentile(samples, 90) * 1e3, "samples": len(samples), "steps_per_sample": g,
+            "kv_gbs": gbs, "frac": gbs / peak, "launches_per_step": step.launches_per_step,
+            "launch_us": phases,
+            "oracle": {"value": cpu["value"], "unit": "GB/s", "cores": cpu["cores"], "sample": cpu["sample"]},
+            "gpu_over_oracle": gbs / cpu["value"] if cpu["value"] > 0 else None,
+        }
+        if name not in reuse:
+            del step, dev
+            torch.cuda.empty_cache()
+    return table, windows
+
+
+# ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
+
+def e2e_breakdown(e2e_step, graph, body, stage_dev, stage_host, res_dev, res_host, step, wall_s, n=50):
+    """Where an end-to-end step's time goes: the H2D copy, the device step
+    and the D2H copy, each timed alone with events; the span one step takes
+    on the device (events around its graph launch); the host time spent in
+    the launch call; and the rest of the wall time (launch latency and the
+    host waking from its wait), as medians in us."""
+    import torch
+
+    def timed(fn, reps=20):
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    h2d = timed(lambda: stage_dev.copy_(stage_host, non_blocking=True))
+    d2h = timed(lambda: res_host.copy_(res_dev, non_blocking=True))
+    dev_step = timed(step.run)
+    spans, launches = [], []
+    for _ in range(n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t = time.perf_counter()
+        a.record()
+        if graph is not None:
+            graph.replay()
+        else:
+            body()
+        b.record()
+        launches.append((time.perf_counter() - t) * 1e6)
+        torch.cuda.synchronize()
+        spans.append(a.elapsed_time(b) * 1e3)
+    span = statistics.median(spans)
+    return {"h2d_us": h2d, "step_us": dev_step, "d2h_us": d2h, "device_span_us": span,
+            "host_launch_call_us": statistics.median(launches),
+            "host_launch_latency_and_wait_us": wall_s * 1e6 - span}
+
 
 def run_ours(args):
     import torch
@@ -400,6 +642,7 @@ def run_ours(args):
         w = wl.with_kv_dtype(w, args.kv_dtype)
     K = args.steps if args.steps is not None else default_steps(w.name)
     W = max(args.warmup, 3)
+    out_dtype = torch.bfloat16 if args.out_dtype == "bf16" else torch.float32
     dev = wl.make_inputs(w, "cuda:%d" % local)
     fused = args.path == "fused" or (args.path == "auto" and not w.shards and not w.shared_prefix
                                      and not w.chunk and args.decode_kernel == "tc")
@@ -409,14 +652,15 @@ def run_ours(args):
     chunk = bool(w.chunk)
     if cascade:
         from paged_kv_decode_kf_gb300.step import CascadeStep
-        step = CascadeStep(dev, suffix_splits=args.num_splits, fused_suffix=args.path != "cascade-calls")
+        step = CascadeStep(dev, suffix_splits=args.num_splits, fused_suffix=args.path != "cascade-calls",
+                           out_dtype=out_dtype)
         kv_bytes = step.unique_kv_bytes()      # the prefix once, each suffix once
     elif chunk:
         from paged_kv_decode_kf_gb300.step import ChunkStep
         step = ChunkStep(dev, num_splits=args.num_splits)
         kv_bytes = dev.kv_bytes()              # each request's cached tokens, once
     else:
-        step = DecodeStep(dev, num_splits=args.num_splits, fused=fused)
+        step = DecodeStep(dev, num_splits=args.num_splits, fused=fused, out_dtype=out_dtype)
         kv_bytes = dev.kv_bytes()
     logical_kv_bytes = dev.kv_bytes()          # sum over requests of their whole context
     stream = torch.cuda.current_stream()
@@ -505,7 +749,6 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     t1 = time.time()
-    clk = clocks.stop(t0, t1)
     ms = start.elapsed_time(end) / K
     phase_source = "events in the timed region (host launches)"
     if graph is not None and not step.fused:
@@ -579,11 +822,12 @@ def run_ours(args):
             else:
                 setattr(dev, n, v)
         if cascade:
-            step_e = CascadeStep(dev, prefix_splits=step.Sp, suffix_splits=step.Ss, fused_suffix=step.fused_suffix)
+            step_e = CascadeStep(dev, prefix_splits=step.Sp, suffix_splits=step.Ss, fused_suffix=step.fused_suffix,
+                                 out_dtype=out_dtype)
         elif chunk:
             step_e = ChunkStep(dev, num_splits=step.S)
         else:
-            step_e = DecodeStep(dev, num_splits=step.num_splits, fused=step.fused)
+            step_e = DecodeStep(dev, num_splits=step.num_splits, fused=step.fused, out_dtype=out_dtype)
         ob = step_e.out.numel() * step_e.out.element_size()
         res_dev = torch.empty(ob + step_e.lse.numel() * 4, dtype=torch.uint8, device=dev.q.device)
         step_e.out = res_dev[:ob].view(step_e.out.dtype).view(step_e.out.shape)
@@ -627,11 +871,19 @@ def run_ours(args):
         te = max_over_ranks(te)
         e2e = {"value": whole_job_gbs(kv_bytes, world, te), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3, "steps": Ke,
+               "out_dtype": args.out_dtype,
                "copies_per_step": "1 H2D (pinned, all inputs) + 1 D2H (out and lse)",
                "launch": "one CUDA graph per step (copies + calls), host waits for the result"
-               if e2e_graph is not None else "host launches, host waits for the result"}
+               if e2e_graph is not None else "host launches, host waits for the result",
+               "breakdown": e2e_breakdown(e2e_step, e2e_graph, e2e_body, stage_dev, stage_host, res_dev, res_host,
+                                          step_e, te)}
 
     peak, peak_src = hbm_peak()
+    per_config, windows = None, []
+    if (world == 1 and not args.no_per_config and args.workload == "ragged" and w.kv_dtype == "bf16"
+            and args.path == "auto" and args.num_splits is None and args.decode_kernel == "tc"):
+        per_config, windows = per_config_table("cuda:%d" % local, out_dtype, {w.name: dev}, peak)
+    clk = clocks.stop(t0, t1, windows)
     att_gbs = kv_bytes / (att_ms * 1e-3) / 1e9
     if cascade:
         # Two kernels carry the step: the shared-prefix pass, a dense contraction
@@ -706,16 +958,20 @@ def run_ours(args):
         cpu = cpu_baseline(w)
 
     if rank == 0:
+        cfg = workload_config(w)
+        # the layout's own count must be what was timed
+        assert cfg["kv_bytes_per_step"] == kv_bytes and cfg["logical_kv_bytes_per_step"] == logical_kv_bytes, (
+            cfg, kv_bytes, logical_kv_bytes)
+        assert cfg["l2"] == l2_note(kv_bytes, dev), (cfg["l2"], l2_note(kv_bytes, dev))
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": ms, "us_per_step": ms * 1e3, "pct_of_hbm_peak": 100.0 * value / world / peak,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8 e4m3 KV, bf16 q",
             "accumulate": "f32", "data": "synthetic",
-            "config": {"workload": w.name + ": " + w.description, "batch": w.batch,
-                       "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                       "block_size": w.block_size, "num_splits": step.num_splits,
-                       "kv_bytes_per_step": kv_bytes, "decode_kernel": args.decode_kernel,
+            "config": cfg,
+            "run": {"num_splits": step.num_splits, "out_dtype": args.out_dtype,
+                       "decode_kernel": args.decode_kernel,
                        "heads_per_cta_override": os.environ.get("KF_TC_HPC"),
                        "num_splits_source": "planner" if args.num_splits is None else "--num-splits",
                        "step": ("chunk attention (multi-query, causal) + LSE merge" if chunk else
@@ -733,13 +989,12 @@ def run_ours(args):
                        "launch": ("CUDA graph replay, %d steps per graph" % g_steps if graph is not None
                                   else "host launches, one step at a time"),
                        "launch_times": phase_source,
-                       "logical_kv_bytes_per_step": logical_kv_bytes,
                        "effective_gbs": logical_kv_bytes / (ms * 1e-3) / 1e9,
-                       "l2": l2_note(kv_bytes, dev),
                        "parallelism": "replica per GPU" if world > 1 else "1 GPU"},
             "roofline": roofline,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "per_config": per_config,
             "clocks": clk,
             "gpu_launches": K * step.launches_per_step,
         }
