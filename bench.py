@@ -67,6 +67,9 @@ def parse():
     ap.add_argument("--no-graph", action="store_true",
                     help="single-launch step: launch each step from the host instead of replaying a "
                          "CUDA graph of consecutive steps")
+    ap.add_argument("--requests", type=int, default=None,
+                    help="run only the first N requests of the workload's seeded draw (their own lengths): "
+                         "a smaller case of the same mix, for profiler captures")
     ap.add_argument("--out-dtype", default="bf16", choices=["bf16", "f32"],
                     help="element type of the step's output rows (the partials and lse stay fp32)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -208,6 +211,7 @@ DIGEST_SOURCES = {
     "decode": ("kf_decode_tc.cuh", "kf_decode_tc.cu", "kf_internal.cuh"),
     "mq5": ("kf_multiquery_tc05.cu", "kf_mq_tc05.cuh", "kf_tc05.cuh", "kf_decode_tc.cuh", "kf_internal.cuh"),
     "mqw": ("kf_multiquery_tc05w.cu", "kf_mq_tc05.cuh", "kf_tc05.cuh", "kf_decode_tc.cuh", "kf_internal.cuh"),
+    "mqp": ("kf_multiquery_tc05p.cu", "kf_mq_tc05.cuh", "kf_tc05.cuh", "kf_decode_tc.cuh", "kf_internal.cuh"),
 }
 
 
@@ -256,6 +260,18 @@ def l2_note(kv_bytes: float, dev) -> str:
     return "inputs fit in L2 (launch-bound case)"
 
 
+def first_requests(w, n: int):
+    """The first `n` requests of workload `w` with the context lengths its
+    seeded draw gives them (same heads, dims, block size and cache type)."""
+    from paged_kv_decode_kf_gb300 import workloads as wl
+    if w.shared_prefix or w.chunk:
+        raise SystemExit("--requests applies to the decode workloads")
+    lay = wl.plan_layout(w)
+    n = max(1, min(n, w.batch))
+    return wl.scaled(w, batch=n, lengths=wl.Fixed(tuple(int(x) for x in lay.ctx_before[:n])),
+                     name=w.name, seed=w.seed, description=w.description + " (first %d requests)" % n)
+
+
 def workload_config(w) -> dict:
     """The `config` object of both arms' JSON lines: the workload and its
     sizes, from the seeded layout alone (so the GPU line and the oracle's
@@ -285,13 +301,14 @@ def workload_config(w) -> dict:
             "l2": l2}
 
 
-def profiled_mq_traffic(workload: str, rows_per_kv_head: int, kv_bytes_per_launch: float):
+def profiled_mq_traffic(workload: str, rows_per_kv_head: int, kv_bytes_per_launch: float, head_dim: int = 128):
     """DRAM traffic of one launch of the tcgen05 multi-query kernel the library
     picks for this many query rows per KV head (the one-tile kernel up to 128,
-    the wide one above), scaled to this launch by its KV bytes; None without a
-    record for `workload` taken from the current sources of that kernel."""
+    above that the CTA-pair kernel at head_dim 128, else the wide one), scaled
+    to this launch by its KV bytes; None without a record for `workload` taken
+    from the current sources of that kernel."""
     path = os.path.join(ROOT, "profiles", "multiquery_dram_traffic.json")
-    kernel = "mq5" if rows_per_kv_head <= 128 else "mqw"
+    kernel = "mq5" if rows_per_kv_head <= 128 else ("mqp" if head_dim == 128 else "mqw")
     try:
         with open(path) as f:
             rec = json.load(f)["kernels"][kernel]
@@ -640,7 +657,9 @@ def run_ours(args):
     w = wl.CONFIGS[args.workload]
     if args.kv_dtype != "bf16":
         w = wl.with_kv_dtype(w, args.kv_dtype)
-    K = args.steps if args.steps is not None else default_steps(w.name)
+    if args.requests is not None:
+        w = first_requests(w, args.requests)
+    K = args.steps if args.steps is not None else default_steps(args.workload)
     W = max(args.warmup, 3)
     out_dtype = torch.bfloat16 if args.out_dtype == "bf16" else torch.float32
     dev = wl.make_inputs(w, "cuda:%d" % local)
@@ -881,6 +900,7 @@ def run_ours(args):
     peak, peak_src = hbm_peak()
     per_config, windows = None, []
     if (world == 1 and not args.no_per_config and args.workload == "ragged" and w.kv_dtype == "bf16"
+            and args.requests is None
             and args.path == "auto" and args.num_splits is None and args.decode_kernel == "tc"):
         per_config, windows = per_config_table("cuda:%d" % local, out_dtype, {w.name: dev}, peak)
     clk = clocks.stop(t0, t1, windows)
@@ -933,7 +953,7 @@ def run_ours(args):
                                  "frac": att_gbs / peak, "algorithmic_bytes_per_launch": kv_bytes,
                                  "peak_source": peak_src + (", of measured" if peak_src.startswith("measured")
                                                             else ", of fallback")}
-        roofline_override.update({"traffic": profiled_mq_traffic(w.name, step.C * w.group, kv_bytes),
+        roofline_override.update({"traffic": profiled_mq_traffic(w.name, step.C * w.group, kv_bytes, w.head_dim),
                                   "kernel": "multi-query attention (chunk queries, causal)",
                                   "flops_per_kv_byte": intensity, "avg_launch_us": att_ms * 1e3,
                                   # no merge launch with one split and fp32 output

@@ -192,7 +192,7 @@ CONFIG_ORDER = ("tiny", "llama8b", "longctx", "shard4", "ragged")
 
 def scaled(w: Workload, *, batch: Optional[int] = None, lengths=None, name=None,
            seed: Optional[int] = None, spare_blocks: Optional[int] = None,
-           kv_dtype: Optional[str] = None) -> Workload:
+           kv_dtype: Optional[str] = None, description: Optional[str] = None) -> Workload:
     """The same heads/dims/block size as `w` with another batch or length mix
     (used for oracle-sized parity cases)."""
     return Workload(
@@ -201,7 +201,8 @@ def scaled(w: Workload, *, batch: Optional[int] = None, lengths=None, name=None,
         block_size=w.block_size, lengths=lengths if lengths is not None else w.lengths,
         seed=seed if seed is not None else w.seed + 7919,
         spare_blocks=w.spare_blocks if spare_blocks is None else spare_blocks,
-        num_splits=w.num_splits, shards=w.shards, description=w.description,
+        num_splits=w.num_splits, shards=w.shards,
+        description=w.description if description is None else description,
         kv_dtype=kv_dtype or w.kv_dtype, shared_prefix=w.shared_prefix, chunk=w.chunk)
 
 
