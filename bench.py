@@ -304,11 +304,10 @@ def workload_config(w) -> dict:
 def profiled_mq_traffic(workload: str, rows_per_kv_head: int, kv_bytes_per_launch: float, head_dim: int = 128):
     """DRAM traffic of one launch of the tcgen05 multi-query kernel the library
     picks for this many query rows per KV head (the one-tile kernel up to 128,
-    above that the CTA-pair kernel at head_dim 128, else the wide one), scaled
-    to this launch by its KV bytes; None without a record for `workload` taken
-    from the current sources of that kernel."""
+    the wide one above), scaled to this launch by its KV bytes; None without a
+    record for `workload` taken from the current sources of that kernel."""
     path = os.path.join(ROOT, "profiles", "multiquery_dram_traffic.json")
-    kernel = "mq5" if rows_per_kv_head <= 128 else ("mqp" if head_dim == 128 else "mqw")
+    kernel = "mq5" if rows_per_kv_head <= 128 else "mqw"
     try:
         with open(path) as f:
             rec = json.load(f)["kernels"][kernel]

@@ -20,7 +20,7 @@ LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libkf.so")
 SOURCES = ["kf_api.cu", "kf_append.cu", "kf_merge.cu", "kf_decode_simt.cu", "kf_decode_tc.cu",
            "kf_decode_tc_fp8.cu", "kf_decode_bal.cu", "kf_decode_bal_fp8.cu", "kf_multiquery.cu",
-           "kf_multiquery_tc05.cu", "kf_multiquery_tc05w.cu", "kf_static.cu"]
+           "kf_multiquery_tc05.cu", "kf_multiquery_tc05w.cu", "kf_multiquery_tc05p.cu", "kf_static.cu"]
 HEADERS = [os.path.join(CSRC, "kf_internal.cuh"), os.path.join(CSRC, "kf_decode_tc.cuh"),
            os.path.join(CSRC, "kf_decode_bal.cuh"),
            os.path.join(CSRC, "kf_tc05.cuh"), os.path.join(CSRC, "kf_mq_tc05.cuh"),

@@ -224,22 +224,26 @@ int decode_impl() {
     return (s && strcmp(s, "simt") == 0) ? 1 : 0;
 }
 
-// Multi-query kernel choice: 0 = mma.sync (32/64-column tiles), 1 = tcgen05
-// with one 128-row query tile and 64-token KV tiles, 2 = tcgen05 with two
-// query tiles and 128-token KV tiles. Two tiles once a request has more than
-// 128 (query, head) rows per KV head, else one: even 8-32 rows (speculative
-// verify of 2-8 tokens at G = 4, HBM-bound) stream KV faster through the
-// one-tile tcgen05 kernel (5.1 TB/s on 64 requests of ~3.8K tokens) than
-// through the mma.sync kernel (4.2 TB/s), the padded rows notwithstanding.
-// KF_MQ_IMPL = "mma", "tc05" or "tc05w" forces one (read per call, so a process
-// can compare them; "tc05w" needs more than 128 rows).
-int multiquery_kernel(int max_query_len, int group) {
+// Which multi-query kernel serves a call: 0 = mma.sync (kf_multiquery.cu), 1 =
+// tcgen05 with one 128-row query tile per CTA, 2 = tcgen05 with two tiles and
+// 128-token KV tiles, 3 = tcgen05 on CTA pairs (head_dim 128 only; opt-in: it
+// measured slower than 2 on the chunked-prefill and cascade workloads). By rows
+// per KV head (max_query_len x group): up to 128 -> 1, more -> 2. Even 8-32 rows (speculative verify of 2-8 tokens at G = 4,
+// HBM-bound) stream KV faster through the one-tile tcgen05 kernel (5.1 TB/s on
+// 64 requests of ~3.8K tokens) than through the mma.sync kernel (4.2 TB/s),
+// the padded rows notwithstanding. KF_MQ_IMPL = "mma", "tc05", "tc05w" or
+// "tc05p" forces one (read per call, so a process can compare them; "tc05w"
+// needs more than 128 rows, and "tc05p" head_dim 128 -- otherwise the default
+// for the shape runs).
+int multiquery_kernel(int max_query_len, int group, int head_dim) {
     const int64_t rows = (int64_t)max_query_len * group;
+    const int wide = rows > 128 ? 2 : 1;
     const char *s = getenv("KF_MQ_IMPL");
     if (s && strcmp(s, "mma") == 0) return 0;
     if (s && strcmp(s, "tc05") == 0) return 1;
     if (s && strcmp(s, "tc05w") == 0) return rows > 128 ? 2 : 1;
-    return rows > 128 ? 2 : 1;
+    if (s && strcmp(s, "tc05p") == 0) return head_dim == 128 ? 3 : wide;
+    return wide;
 }
 
 }  // namespace kf
@@ -445,9 +449,10 @@ kf_status kf_paged_multiquery_attention(const void *q, const int32_t *q_start, c
     p.scale_log2 = scale * 1.4426950408889634f;
     void *fn = encode_fn();
     if (!fn) return KF_ERR_CUDA;
-    const int which = multiquery_kernel(max_query_len, num_q_heads / num_kv_heads);
+    const int which = multiquery_kernel(max_query_len, num_q_heads / num_kv_heads, head_dim);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = which == 2   ? launch_multiquery_tc05w(p, st, fn)
+    const cudaError_t e = which == 3   ? launch_multiquery_tc05p(p, st, fn)
+                          : which == 2 ? launch_multiquery_tc05w(p, st, fn)
                           : which == 1 ? launch_multiquery_tc05(p, st, fn)
                                        : launch_multiquery(p, st, fn);
     if (e == cudaErrorInvalidValue) return KF_ERR_UNSUPPORTED;

@@ -75,6 +75,8 @@ cudaError_t launch_multiquery(MqParams p, cudaStream_t stream, void *encode_fn);
 cudaError_t launch_multiquery_tc05(MqParams p, cudaStream_t stream, void *encode_fn);
 // tcgen05, 128-token KV tiles and two query tiles per CTA (> 128 rows per KV head).
 cudaError_t launch_multiquery_tc05w(MqParams p, cudaStream_t stream, void *encode_fn);
+// tcgen05 on CTA pairs (cta_group::2, M = 256 across two SMs), head_dim 128.
+cudaError_t launch_multiquery_tc05p(MqParams p, cudaStream_t stream, void *encode_fn);
 
 // Decode kernels, one per implementation. Each returns the launch status.
 cudaError_t launch_decode_simt(const DecodeParams &p, cudaStream_t stream);

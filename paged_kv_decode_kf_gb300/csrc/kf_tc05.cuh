@@ -159,5 +159,51 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// CTA pairs (cta_group::2). Two CTAs of a cluster whose ranks differ in bit 0
+// issue MMAs together: one thread of the even CTA issues; A's rows are split
+// between the two CTAs (rows 0-127 in the even CTA's shared memory or TMEM,
+// 128-255 in the odd one's, at the same addresses), B's N columns likewise
+// (the first N/2 in the even CTA), and D's rows land in each CTA's own TMEM.
+// Every tcgen05 instruction of a kernel that uses them must be of this form.
+// ---------------------------------------------------------------------------
+
+// Allocation of `ncols` columns in both CTAs' TMEM, by one warp of each CTA.
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void mma2_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma2_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// One arrival on the mbarrier at offset `bar` of every CTA in `cta_mask` once
+// every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void commit2(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
 }  // namespace tc05
 }  // namespace kf

@@ -42,8 +42,8 @@ def decode_impl(name: str):
 def mq_impl(name: str):
     """Select the multi-query kernel for the calls in the block: "mma", "tc05"
     (one 128-row query tile per CTA), "tc05x2" (two tiles per CTA, 64-token KV
-    tiles), "tc05w" (two tiles, 128-token KV tiles; more than 128 rows) or
-    "auto"."""
+    tiles), "tc05w" (two tiles, 128-token KV tiles; more than 128 rows),
+    "tc05p" (CTA pairs, head_dim 128; any row count) or "auto"."""
     with _env("KF_MQ_IMPL", "tc05" if name == "tc05x2" else name), \
             _env("KF_MQ_TILES", "2" if name == "tc05x2" else "1"):
         yield

@@ -50,7 +50,7 @@ CASES = {
 }
 
 
-IMPLS = ["mma", "tc05", "tc05x2", "tc05w"]
+IMPLS = ["mma", "tc05", "tc05x2", "tc05w", "tc05p"]
 
 
 @pytest.mark.parametrize("impl", IMPLS)
