@@ -52,6 +52,9 @@
 // Precision: scores and O accumulate in fp32; P enters the PV product as
 // bf16 (relative error <= 2^-9 per weight, unbiased rounding), l sums the
 // unrounded fp32 weights.
+#include <stdlib.h>
+#include <string.h>
+
 #include "kf_mq_tc05.cuh"
 
 namespace kf {
@@ -76,8 +79,11 @@ struct T5Shape {
     static constexpr int kSlots = (QT == 1 ? 4 : 8) * (128 / D);
     static constexpr int kSmemBytes = kQBytes + kSlots * kSlotBytes + 1024;
     static constexpr int kSoftWarps = 4 * QT;
-    static constexpr int kProducer = kSoftWarps, kIssuer = kSoftWarps + 1;
-    static constexpr int kThreads = 32 * (kSoftWarps + 2);
+    // NPW TMA producer warps: kProducer (K items, or every item when NPW = 1)
+    // and kProducer2 (V items). TMA instructions issued by the lanes of one warp
+    // are taken one after another (~90 cycles per box); different warps' overlap.
+    static constexpr int kProducer = kSoftWarps, kIssuer = kSoftWarps + 1, kProducer2 = kSoftWarps + 2;
+    __host__ __device__ static constexpr int threads(int npw) { return 32 * (kSoftWarps + 1 + npw); }
     // TMEM columns: S_t [64 t, +64), P_t two buffers of 32 at 64 QT + 64 t,
     // O_t D columns at 128 QT + D t
     static constexpr uint32_t kTmemCols = QT == 1 ? 256 : 512;
@@ -90,8 +96,12 @@ struct T5Shape {
 };
 
 
-template <int D, int G, int QT>
-__global__ void __launch_bounds__(T5Shape<D, QT>::kThreads, QT == 1 ? 2 : 1)
+// Two CTAs per SM with one tile (one with two). A sub-partition's 16384
+// registers hold floor(16384 / (32 x regs)) warps, so two seven-warp CTAs (four
+// warps on some sub-partitions) cap a thread at 128 registers; at that cap the
+// kernel spills a few bytes, which measured faster than one CTA per SM.
+template <int D, int G, int QT, int NPW>
+__global__ void __launch_bounds__(T5Shape<D, QT>::threads(NPW), QT == 1 ? 2 : 1)
 mq5_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
            const __grid_constant__ CUtensorMap tmap_v) {
     using Sh = T5Shape<D, QT>;
@@ -193,19 +203,21 @@ mq5_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     tc05::fence_after_sync();
     const uint32_t tm = tmem_slot;
 
-    if (warp == Sh::kProducer) {
+    if (warp == Sh::kProducer || (NPW == 2 && warp == Sh::kProducer2)) {
         // ------------------------------ producer ------------------------------
-        // The whole warp walks the tiles: the table entries come 32 at a time
+        // (with two producer warps, warp kProducer takes the K items 2j and
+        // warp kProducer2 the V items 2j + 1)
+        // The whole warp walks its items: the table entries come 32 at a time
         // (one coalesced load, lane e holds logical block base + e), so no TMA
         // issue waits on a dependent load; lane 0 waits for slots, and lane k
-        // issues the box of the tile's block k (issues from one lane, one
-        // after another, cost a few hundred cycles each).
+        // issues the box of the tile's block k.
         const int bs_shift = block_shift(p.block_size);
         const uint32_t box_bytes = (uint32_t)p.block_size * D * 2;
+        const int ifirst = warp == Sh::kProducer ? 0 : 1, istep = NPW;
         int64_t tab_base = -1;
         int32_t tab_ent = -1;
         int issued = 0;
-        for (int i = 0; i < 2 * ntiles; ++i) {
+        for (int i = ifirst; i < 2 * ntiles; i += istep) {
             const int slot = i % NSL;
             int go = 1;
             if (lane == 0) {
@@ -233,16 +245,18 @@ mq5_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
                     raise_error(p.err, KF_DEVERR_BLOCK_ID);
                     phys = 0;
                 }
-                tma_load_5d(sKV + slot * Sh::kSlotBytes + lane * box_bytes, map, 0, 0, h * Sh::kHalves, 0,
-                            (int)phys, full(slot));
+                tma_load_4d(sKV + slot * Sh::kSlotBytes + lane * box_bytes, map, 0, 0, h * Sh::kHalves,
+                            (int)phys * (p.block_size / 8), full(slot));
             }
             __syncwarp();
             issued = i + 1;
         }
         if (lane == 0) {
-            // drain: the copies of the last NSL issues have landed before the CTA can exit
+            // drain: this warp's copies among the last NSL items have landed
+            // before the CTA can exit
             for (int i = issued > NSL ? issued - NSL : 0; i < issued; ++i)
-                if (!mbar_wait(full(i % NSL), (i / NSL) & 1)) raise_error(p.err, KF_DEVERR_TIMEOUT);
+                if ((i - ifirst) % istep == 0 && !mbar_wait(full(i % NSL), (i / NSL) & 1))
+                    raise_error(p.err, KF_DEVERR_TIMEOUT);
         }
     } else if (warp == Sh::kIssuer) {
         // ------------------------------ MMA issuer -----------------------------
@@ -496,7 +510,7 @@ mq5_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     }
 }
 
-template <int D, int G, int QT>
+template <int D, int G, int QT, int NPW>
 cudaError_t launch_t5(const MqParams &p, cudaStream_t stream, const CUtensorMap &mk, const CUtensorMap &mv) {
     using Sh = T5Shape<D, QT>;
     static std::atomic<uint64_t> done{0};
@@ -505,14 +519,23 @@ cudaError_t launch_t5(const MqParams &p, cudaStream_t stream, const CUtensorMap 
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(done.load() & bit)) {
-        e = cudaFuncSetAttribute(mq5_kernel<D, G, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(mq5_kernel<D, G, QT, NPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Sh::kSmemBytes);
         if (e != cudaSuccess) return e;
         done.fetch_or(bit);
     }
     const dim3 grid(p.num_splits, p.num_kv_heads, p.batch * p.q_tiles);
-    mq5_kernel<D, G, QT><<<grid, Sh::kThreads, Sh::kSmemBytes, stream>>>(p, mk, mv);
+    mq5_kernel<D, G, QT, NPW><<<grid, Sh::threads(NPW), Sh::kSmemBytes, stream>>>(p, mk, mv);
     return cudaGetLastError();
+}
+
+// Two producer warps by default; KF_MQW_PRODUCERS = 1 selects one (read per
+// call, for comparisons).
+template <int D, int G, int QT>
+cudaError_t launch_t5(const MqParams &p, cudaStream_t stream, const CUtensorMap &mk, const CUtensorMap &mv) {
+    const char *s = getenv("KF_MQW_PRODUCERS");
+    if (s && strcmp(s, "1") == 0) return launch_t5<D, G, QT, 1>(p, stream, mk, mv);
+    return launch_t5<D, G, QT, 2>(p, stream, mk, mv);
 }
 
 template <int D, int QT>

@@ -81,8 +81,10 @@ struct PShape {
     static constexpr int kSlotBytes = 16 * 1024;  // 64 tokens x 128 d, or 128 tokens x 64 d
     static constexpr int kSlots = 12;
     static constexpr int kSmemBytes = kQBytes + kSlots * kSlotBytes + 1024;
-    static constexpr int kThreads = 320;
-    static constexpr int kProducer = 8, kIssuer = 9;
+    static constexpr int kThreads = 352;
+    // TMA producers: warp 8 the K halves, warp 10 the V halves (TMA instructions
+    // from one warp's lanes are taken one after another; different warps' overlap)
+    static constexpr int kProducer = 8, kIssuer = 9, kProducer2 = 10;
     static constexpr uint32_t kTmemCols = 512;
     __host__ __device__ static constexpr uint32_t col_s(int w) { return 128u * w; }
     __host__ __device__ static constexpr uint32_t col_o(int w) { return 256u + 128u * w; }
@@ -91,57 +93,8 @@ struct PShape {
     static_assert(kRowsP * kDP * 4 + 4 * kRowsP * 4 <= kSlots * kSlotBytes, "epilogue staging");
 };
 
-// ----------------------------------------------------------------------------
-// Cluster (pair) primitives
-// ----------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-
-// One arrival on an mbarrier of any CTA of the cluster (`caddr` from map_to).
-__device__ __forceinline__ void arrive_cluster(uint32_t caddr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
-
-__device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait on a local barrier whose arrivals may come from the other CTA.
-__device__ __forceinline__ bool wait_cl(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kMaxSpins; ++i)
-        if (try_wait_cluster(bar, parity)) return true;
-    return false;
-}
-
-__device__ __forceinline__ bool warp_wait_cl(uint32_t bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, wait_cl(bar, parity));
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 template <int G>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
 mqp_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
            const __grid_constant__ CUtensorMap tmap_vh) {
     using Sh = PShape;
@@ -173,7 +126,8 @@ mqp_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     const int bs_shift = block_shift(p.block_size);
     int64_t tab_base = -1;
     int32_t tab_ent = -1;
-    if (warp == Sh::kProducer) {
+    const bool producer = warp == Sh::kProducer || warp == Sh::kProducer2;
+    if (producer) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_vh)) : "memory");
@@ -259,13 +213,15 @@ mqp_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     const uint32_t tm = tmem_slot;
     const uint16_t both = 0x3;
 
-    if (warp == Sh::kProducer) {
-        // ------------------------------ producer ------------------------------
-        // Items i = 2j (K half of tile j) and 2j + 1 (V half), in order, slot i % NSL.
+    if (producer) {
+        // ------------------------------ producers -----------------------------
+        // Items i = 2j (K half of tile j; warp kProducer) and 2j + 1 (V half;
+        // warp kProducer2), each warp's in order, slot i % NSL.
         const uint32_t kbox = (uint32_t)p.block_size * D * 2;   // one block, all 128 columns
         const uint32_t vbox = (uint32_t)p.block_size * 64 * 2;  // one block, 64 columns
+        const int ifirst = warp == Sh::kProducer ? 0 : 1;
         int issued = 0;
-        for (int i = 0; i < 2 * ntiles; ++i) {
+        for (int i = ifirst; i < 2 * ntiles; i += 2) {
             const int slot = i % NSL;
             int go = 1;
             if (lane == 0) {
@@ -306,19 +262,22 @@ mqp_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
                         phys = 0;
                     }
                     const uint32_t dst = sKV + slot * Sh::kSlotBytes + lane * (isv ? vbox : kbox);
+                    const int grp = (int)phys * (p.block_size / 8);
                     if (isv)
-                        tma_load_5d(dst, &tmap_vh, 0, 0, h * 2 + (int)cr, 0, (int)phys, full(slot));
+                        tma_load_4d(dst, &tmap_vh, 0, 0, h * 2 + (int)cr, grp, full(slot));
                     else
-                        tma_load_5d(dst, &tmap_k, 0, 0, h * 2, 0, (int)phys, full(slot));
+                        tma_load_4d(dst, &tmap_k, 0, 0, h * 2, grp, full(slot));
                 }
             }
             __syncwarp();
             issued = i + 1;
         }
         if (lane == 0) {
-            // drain: the copies of the last NSL issues have landed before the CTA can exit
+            // drain: this warp's copies among the last NSL items have landed
+            // before the CTA can exit
             for (int i = issued > NSL ? issued - NSL : 0; i < issued; ++i)
-                if (!mbar_wait(full(i % NSL), (i / NSL) & 1)) raise_error(p.err, KF_DEVERR_TIMEOUT);
+                if (((i - ifirst) & 1) == 0 && !mbar_wait(full(i % NSL), (i / NSL) & 1))
+                    raise_error(p.err, KF_DEVERR_TIMEOUT);
         }
     } else if (warp == Sh::kIssuer && cr == 1) {
         // --------------------- relay (odd CTA): loads landed ---------------------
@@ -616,18 +575,18 @@ mqp_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     }
 }
 
-// 5-D view of a [num_blocks, bs, Hkv, 128] bf16 cache whose box is one block
-// of one head's 64-column half: (d % 64, slot % 8, head * 2 + d / 64, slot / 8,
-// block), box (64, 8, 1, bs / 8, 1) = bs * 128 bytes, landing as 8-token atoms
-// of 128-byte rows (token t at (t / 8) * 1024 + (t % 8) * 128).
+// 4-D view of a [num_blocks, bs, Hkv, 128] bf16 cache whose box is one block
+// of one head's 64-column half: (d % 64, slot % 8, head * 2 + d / 64, 8-slot
+// group = block * bs/8 + slot / 8), box (64, 8, 1, bs / 8) = bs * 128 bytes,
+// landing as 8-token atoms of 128-byte rows (token t at (t / 8) * 1024 +
+// (t % 8) * 128).
 bool encode_half_map(tc::EncodeFn fn, CUtensorMap *map, const void *cache, const MqParams &p) {
     const cuuint64_t row = (cuuint64_t)p.num_kv_heads * p.head_dim * 2;  // bytes between slots
-    const cuuint64_t dims[5] = {64, 8, (cuuint64_t)p.num_kv_heads * 2, (cuuint64_t)p.block_size / 8,
-                                (cuuint64_t)p.num_blocks};
-    const cuuint64_t strides[4] = {row, 128, 8 * row, row * p.block_size};
-    const cuuint32_t box[5] = {64, 8, 1, (cuuint32_t)p.block_size / 8, 1};
-    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(cache), dims, strides, box, estr,
+    const cuuint64_t dims[4] = {64, 8, (cuuint64_t)p.num_kv_heads * 2, (cuuint64_t)p.num_blocks * (p.block_size / 8)};
+    const cuuint64_t strides[3] = {row, 128, 8 * row};
+    const cuuint32_t box[4] = {64, 8, 1, (cuuint32_t)p.block_size / 8};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(cache), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

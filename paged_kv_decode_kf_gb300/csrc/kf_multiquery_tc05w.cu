@@ -50,6 +50,9 @@
 //
 // Precision: scores and O accumulate in fp32; P enters the PV product as bf16
 // (relative error <= 2^-9 per weight); l sums the unrounded fp32 weights.
+#include <stdlib.h>
+#include <string.h>
+
 #include "kf_mq_tc05.cuh"
 
 namespace kf {
@@ -73,8 +76,11 @@ struct WShape {
     // is about a microsecond, a tile's MMAs take under one): 5 x 32 KiB at D 128
     static constexpr int kSlots = D == 128 ? 5 : 12;
     static constexpr int kSmemBytes = kQBytes + kSlots * kSlotBytes + 1024;
-    static constexpr int kThreads = 320;
-    static constexpr int kProducer = 8, kIssuer = 9;
+    // NPW TMA producer warps: warp 8 (K items, or every item when NPW = 1) and
+    // warp 10 (V items). TMA instructions issued by the lanes of one warp are
+    // taken one after another (~90 cycles per box); different warps' overlap.
+    static constexpr int threads(int npw) { return npw == 2 ? 352 : 320; }
+    static constexpr int kProducer = 8, kIssuer = 9, kProducer2 = 10;
     static constexpr uint32_t kTmemCols = 512;
     __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
     __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + (uint32_t)D * t; }
@@ -83,8 +89,8 @@ struct WShape {
     static_assert(2 * kRowsW * D * 4 <= kSlots * kSlotBytes, "the ring holds both tiles' output rows");
 };
 
-template <int D, int G>
-__global__ void __launch_bounds__(320, 1)
+template <int D, int G, int NPW>
+__global__ void __launch_bounds__(NPW == 2 ? 352 : 320, 1)
 mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
            const __grid_constant__ CUtensorMap tmap_v) {
     using Sh = WShape<D>;
@@ -102,6 +108,13 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     const uint32_t bars = smem_u32(bar_mem);
     auto full = [&](int i) { return bars + 8u * i; };
     auto empty = [&](int i) { return bars + 8u * (NSL + i); };
+    // The ring is two rings: K tiles in slots [0, NK), V tiles in [NK, NSL). Each
+    // kind's items reuse only their own slots, in order, so a producer warp that
+    // runs ahead of the other can never wait on a slot whose previous item the
+    // other warp has yet to issue (a parity wait would then alias).
+    constexpr int NK = (NSL + 1) / 2, NV = NSL - NK;
+    auto slot_of = [](int i) { return (i & 1) ? NK + (i >> 1) % NV : (i >> 1) % NK; };
+    auto phase_of = [](int i) -> uint32_t { return ((i & 1) ? (i >> 1) / NV : (i >> 1) / NK) & 1; };
     const uint32_t q_ready = bars + 8u * (2 * NSL), fin = q_ready + 8;
     auto s_full = [&](int t) { return fin + 8u + 8u * t; };
     auto p_full = [&](int t) { return fin + 24u + 8u * t; };
@@ -119,7 +132,8 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     const int bs_shift = block_shift(p.block_size);
     int64_t tab_base = -1;
     int32_t tab_ent = -1;
-    if (warp == Sh::kProducer) {
+    const bool producer = warp == Sh::kProducer || (NPW == 2 && warp == Sh::kProducer2);
+    if (producer) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
@@ -198,18 +212,20 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     __syncthreads();
     tc05::fence_after_sync();
     const uint32_t tm = tmem_slot;
-    if (warp == Sh::kProducer) {
+    if (producer) {
         // ------------------------------ producer ------------------------------
-        // The whole warp walks the tiles: table entries come 32 at a time (one
-        // coalesced load, lane e holds logical block base + e); lane 0 waits
-        // for slots and lane k issues the box of the tile's block k.
+        // The whole warp walks its items (K_j = item 2j, V_j = item 2j + 1; with
+        // two producer warps each takes one kind): table entries come 32 at a
+        // time (one coalesced load, lane e holds logical block base + e); lane 0
+        // waits for slots and lane k issues the box of the tile's block k.
         const uint32_t box_bytes = (uint32_t)p.block_size * D * 2;
-        int issued = 0;
-        for (int i = 0; i < 2 * ntiles; ++i) {
-            const int slot = i % NSL;
+        const int ifirst = warp == Sh::kProducer ? 0 : 1, istep = NPW;
+        int last_k = -1, last_v = -1;  // this warp's last K / V tile issued
+        for (int i = ifirst; i < 2 * ntiles; i += istep) {
+            const int slot = slot_of(i);
             int go = 1;
             if (lane == 0) {
-                go = !abort_flag && mbar_wait(empty(slot), ((i / NSL) & 1) ^ 1);
+                go = !abort_flag && mbar_wait(empty(slot), phase_of(i) ^ 1);
                 if (!go) {
                     raise_error(p.err, KF_DEVERR_TIMEOUT);
                     abort_flag = 1;
@@ -233,16 +249,19 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
                     raise_error(p.err, KF_DEVERR_BLOCK_ID);
                     phys = 0;
                 }
-                tma_load_5d(sKV + slot * Sh::kSlotBytes + lane * box_bytes, map, 0, 0, h * Sh::kHalves, 0,
-                            (int)phys, full(slot));
+                tma_load_4d(sKV + slot * Sh::kSlotBytes + lane * box_bytes, map, 0, 0, h * Sh::kHalves,
+                            (int)phys * (p.block_size / 8), full(slot));
             }
             __syncwarp();
-            issued = i + 1;
+            (i & 1 ? last_v : last_k) = i >> 1;
         }
         if (lane == 0) {
-            // drain: the copies of the last NSL issues have landed before the CTA can exit
-            for (int i = issued > NSL ? issued - NSL : 0; i < issued; ++i)
-                if (!mbar_wait(full(i % NSL), (i / NSL) & 1)) raise_error(p.err, KF_DEVERR_TIMEOUT);
+            // drain: the last use of each slot this warp filled has landed
+            // before the CTA can exit
+            for (int j = last_k - NK + 1 > 0 ? last_k - NK + 1 : 0; j <= last_k; ++j)
+                if (!mbar_wait(full(slot_of(2 * j)), phase_of(2 * j))) raise_error(p.err, KF_DEVERR_TIMEOUT);
+            for (int j = last_v - NV + 1 > 0 ? last_v - NV + 1 : 0; j <= last_v; ++j)
+                if (!mbar_wait(full(slot_of(2 * j + 1)), phase_of(2 * j + 1))) raise_error(p.err, KF_DEVERR_TIMEOUT);
         }
     } else if (warp == Sh::kIssuer) {
         // ------------------------------ MMA issuer -----------------------------
@@ -259,9 +278,9 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
                     break;
                 }
                 const bool has_s = j < ntiles, has_pv = j > 0;
-                const int kslot = (2 * j) % NSL, vslot = (2 * j + NSL - 1) % NSL;
-                if ((has_s && !mbar_wait(full(kslot), ((2 * j) / NSL) & 1)) ||
-                    (has_pv && !mbar_wait(full(vslot), ((2 * j - 1) / NSL) & 1))) {
+                const int kslot = slot_of(2 * j), vslot = has_pv ? slot_of(2 * j - 1) : 0;
+                if ((has_s && !mbar_wait(full(kslot), phase_of(2 * j))) ||
+                    (has_pv && !mbar_wait(full(vslot), phase_of(2 * j - 1)))) {
                     ok = false;
                     break;
                 }
@@ -345,8 +364,8 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
                 const int64_t ntile_tok = t_hi - t0 < kTileW ? t_hi - t0 : kTileW;
                 if (ntile_tok < kTileW) {
                     // zero the V rows past the range (each tile's warps zero all of them)
-                    const int slot = (2 * j + 1) % NSL;
-                    if (!warp_wait(full(slot), ((2 * j + 1) / NSL) & 1)) {
+                    const int slot = slot_of(2 * j + 1);
+                    if (!warp_wait(full(slot), phase_of(2 * j + 1))) {
                         ok = false;
                         break;
                     }
@@ -494,7 +513,7 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     }
 }
 
-template <int D, int G>
+template <int D, int G, int NPW>
 cudaError_t launch_w(const MqParams &p, cudaStream_t stream, const CUtensorMap &mk, const CUtensorMap &mv) {
     using Sh = WShape<D>;
     static std::atomic<uint64_t> done{0};
@@ -503,13 +522,23 @@ cudaError_t launch_w(const MqParams &p, cudaStream_t stream, const CUtensorMap &
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(done.load() & bit)) {
-        e = cudaFuncSetAttribute(mqw_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmemBytes);
+        e = cudaFuncSetAttribute(mqw_kernel<D, G, NPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Sh::kSmemBytes);
         if (e != cudaSuccess) return e;
         done.fetch_or(bit);
     }
     const dim3 grid(p.num_splits, p.num_kv_heads, p.batch * p.q_tiles);
-    mqw_kernel<D, G><<<grid, Sh::kThreads, Sh::kSmemBytes, stream>>>(p, mk, mv);
+    mqw_kernel<D, G, NPW><<<grid, Sh::threads(NPW), Sh::kSmemBytes, stream>>>(p, mk, mv);
     return cudaGetLastError();
+}
+
+// Two producer warps by default; KF_MQW_PRODUCERS = 1 selects one (read per
+// call, for comparisons).
+template <int D, int G>
+cudaError_t launch_w(const MqParams &p, cudaStream_t stream, const CUtensorMap &mk, const CUtensorMap &mv) {
+    const char *s = getenv("KF_MQW_PRODUCERS");
+    if (s && strcmp(s, "1") == 0) return launch_w<D, G, 1>(p, stream, mk, mv);
+    return launch_w<D, G, 2>(p, stream, mk, mv);
 }
 
 template <int D>
