@@ -335,20 +335,18 @@ mqp_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
                 }
             }
             for (int j = 0; ok && j < ntiles; ++j) {
-                if (abort_flag || !wait_cl(p_full(j & 1), (j >> 1) & 1) || !ready(2 * j + 1)) {
+                // V_j and K_{j+2} are normally loaded long before the softmax of
+                // tile j is done: wait for them first, so that PV_j and S_{j+2}
+                // go out back to back once it is (their slots' previous items
+                // were consumed steps ago, so these waits need nothing from step j)
+                if (abort_flag || !ready(2 * j + 1) || (j + 2 < ntiles && !ready(2 * (j + 2))) ||
+                    !wait_cl(p_full(j & 1), (j >> 1) & 1)) {
                     ok = false;
                     break;
                 }
                 tc05::fence_after_sync();
                 issue_pv(j);
-                if (j + 2 < ntiles) {
-                    if (!ready(2 * (j + 2))) {
-                        ok = false;
-                        break;
-                    }
-                    tc05::fence_after_sync();
-                    issue_s(j + 2);
-                }
+                if (j + 2 < ntiles) issue_s(j + 2);
             }
             if (!ok) {
                 raise_error(p.err, KF_DEVERR_TIMEOUT);
