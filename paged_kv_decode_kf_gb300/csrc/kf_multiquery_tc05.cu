@@ -68,15 +68,23 @@ constexpr int kTile = 64;   // tokens per KV tile
 
 // Shared-memory and TMEM geometry of a CTA with QT query tiles (QT = 2: both
 // tiles read every K/V tile once, one CTA per SM; QT = 1: two CTAs per SM).
-template <int D, int QT>
+// SQ (compact Q, one tile): a request has at most 32 rows per KV head
+// (speculative verify: 4 draft tokens x G 4 = 16). Only those rows of Q are
+// stored (8 KiB at D 128 instead of 32); the MMA still reads 128 rows of A, and
+// the rows past the stored ones read whatever the ring holds there -- they
+// only make rows of S, P and O that no warp reads or stores (an MMA row
+// depends on its own row of A alone). The room goes to two more ring slots.
+template <int D, int QT, bool SQ = false>
 struct T5Shape {
     static constexpr int kHalves = D / 64;                       // 64-wide d halves (128-byte rows)
-    static constexpr int kQHalfBytes = kRows * 128;              // 16 KiB
+    static constexpr int kQRows = SQ ? 32 : kRows;               // rows of Q stored
+    static constexpr int kQHalfBytes = kQRows * 128;             // 16 KiB (4 KiB compact)
     static constexpr int kQTileBytes = kHalves * kQHalfBytes;
     static constexpr int kQBytes = QT * kQTileBytes;
     static constexpr int kAtomBytes = kHalves * 1024;            // 8 tokens x D
     static constexpr int kSlotBytes = kTile / 8 * kAtomBytes;    // 64 tokens x D
-    static constexpr int kSlots = (QT == 1 ? 4 : 8) * (128 / D);
+    static constexpr int kSlots = (QT == 1 ? (SQ ? 6 : 4) : 8) * (128 / D);
+    static_assert(!SQ || QT == 1, "compact Q has one tile");
     static constexpr int kSmemBytes = kQBytes + kSlots * kSlotBytes + 1024;
     static constexpr int kSoftWarps = 4 * QT;
     // NPW TMA producer warps: kProducer (K items, or every item when NPW = 1)
@@ -100,11 +108,11 @@ struct T5Shape {
 // registers hold floor(16384 / (32 x regs)) warps, so two seven-warp CTAs (four
 // warps on some sub-partitions) cap a thread at 128 registers; at that cap the
 // kernel spills a few bytes, which measured faster than one CTA per SM.
-template <int D, int G, int QT, int NPW>
-__global__ void __launch_bounds__(T5Shape<D, QT>::threads(NPW), QT == 1 ? 2 : 1)
+template <int D, int G, int QT, int NPW, bool SQ>
+__global__ void __launch_bounds__(T5Shape<D, QT, SQ>::threads(NPW), QT == 1 ? 2 : 1)
 mq5_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
            const __grid_constant__ CUtensorMap tmap_v) {
-    using Sh = T5Shape<D, QT>;
+    using Sh = T5Shape<D, QT, SQ>;
     constexpr int NSL = Sh::kSlots;
     constexpr int KS = D / 16;  // K steps of S = Q K^T
 
@@ -335,6 +343,7 @@ mq5_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
             const uint32_t qb = sQ + tq * Sh::kQTileBytes;
 #pragma unroll
             for (int c16 = 0; c16 < D / 8; ++c16) {
+                if (r >= Sh::kQRows) break;  // compact Q: rows past the stored ones
                 const uint4 v = row_ok ? __ldg(src + c16) : make_uint4(0u, 0u, 0u, 0u);
                 const uint32_t a = qb + (c16 >> 3) * Sh::kQHalfBytes + (r >> 3) * 1024 + (r & 7) * 128 +
                                    (((c16 & 7) ^ (r & 7)) << 4);
@@ -510,32 +519,40 @@ mq5_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     }
 }
 
-template <int D, int G, int QT, int NPW>
+template <int D, int G, int QT, int NPW, bool SQ>
 cudaError_t launch_t5(const MqParams &p, cudaStream_t stream, const CUtensorMap &mk, const CUtensorMap &mv) {
-    using Sh = T5Shape<D, QT>;
+    using Sh = T5Shape<D, QT, SQ>;
     static std::atomic<uint64_t> done{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = 1ull << (dev & 63);
     if (!(done.load() & bit)) {
-        e = cudaFuncSetAttribute(mq5_kernel<D, G, QT, NPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(mq5_kernel<D, G, QT, NPW, SQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Sh::kSmemBytes);
         if (e != cudaSuccess) return e;
         done.fetch_or(bit);
     }
     const dim3 grid(p.num_splits, p.num_kv_heads, p.batch * p.q_tiles);
-    mq5_kernel<D, G, QT, NPW><<<grid, Sh::threads(NPW), Sh::kSmemBytes, stream>>>(p, mk, mv);
+    mq5_kernel<D, G, QT, NPW, SQ><<<grid, Sh::threads(NPW), Sh::kSmemBytes, stream>>>(p, mk, mv);
     return cudaGetLastError();
 }
 
-// Two producer warps by default; KF_MQW_PRODUCERS = 1 selects one (read per
-// call, for comparisons).
+// Compact Q when a request has at most 32 rows per KV head, with one producer
+// warp: its six-slot ring keeps enough in flight, and at two CTAs per SM a
+// seventh warp would cap a thread at 128 registers and spill (speculative
+// verify: 162.5 us against 167.7 with two producers, 170.3 without compact Q).
+// Otherwise two producer warps (181.8 -> 168.5 us there before compact Q).
+// KF_MQW_PRODUCERS = 1 or 2 and KF_MQ_COMPACT_Q = 0 override (read per call).
 template <int D, int G, int QT>
 cudaError_t launch_t5(const MqParams &p, cudaStream_t stream, const CUtensorMap &mk, const CUtensorMap &mv) {
     const char *s = getenv("KF_MQW_PRODUCERS");
-    if (s && strcmp(s, "1") == 0) return launch_t5<D, G, QT, 1>(p, stream, mk, mv);
-    return launch_t5<D, G, QT, 2>(p, stream, mk, mv);
+    const char *c = getenv("KF_MQ_COMPACT_Q");
+    const bool sq = QT == 1 && (int64_t)p.max_query_len * G <= 32 && !(c && strcmp(c, "0") == 0);
+    const bool one = s ? strcmp(s, "1") == 0 : sq;
+    if (QT == 1 && sq)
+        return one ? launch_t5<D, G, 1, 1, true>(p, stream, mk, mv) : launch_t5<D, G, 1, 2, true>(p, stream, mk, mv);
+    return one ? launch_t5<D, G, QT, 1, false>(p, stream, mk, mv) : launch_t5<D, G, QT, 2, false>(p, stream, mk, mv);
 }
 
 template <int D, int QT>
