@@ -597,22 +597,25 @@ def per_config_table(device: str, out_dtype, reuse: dict, peak: float, oracle_s:
 
 def e2e_breakdown(e2e_step, graph, body, stage_dev, stage_host, res_dev, res_host, step, wall_s, n=50):
     """Where an end-to-end step's time goes: the H2D copy, the device step
-    and the D2H copy, each timed alone with events; the span one step takes
+    and the D2H copy, each timed alone with events (enqueued ahead, behind a
+    stream sleep); the span one step takes
     on the device (events around its graph launch); the host time spent in
     the launch call; and the rest of the wall time (launch latency and the
     host waking from its wait), as medians in us."""
     import torch
 
     def timed(fn, reps=20):
-        ts = []
-        for _ in range(reps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # enqueued behind a stream sleep, so the events bracket device time only
+        # (not the host's enqueue of each copy or launch)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(10_000_000)
+        for a, b in evs:
             a.record()
             fn()
             b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b) * 1e3)
-        return statistics.median(ts)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
 
     h2d = timed(lambda: stage_dev.copy_(stage_host, non_blocking=True))
     d2h = timed(lambda: res_host.copy_(res_dev, non_blocking=True))
