@@ -64,6 +64,8 @@ def parse():
     ap.add_argument("--num-splits", type=int, default=None,
                     help="override the planner's split count (tuning sweeps); 0 = the balanced one-wave "
                          "schedule of the single-launch step (fused and cascade paths)")
+    ap.add_argument("--prefix-splits", type=int, default=None,
+                    help="cascade workloads: split count of the shared-prefix pass (default: one wave of CTAs)")
     ap.add_argument("--no-graph", action="store_true",
                     help="single-launch step: launch each step from the host instead of replaying a "
                          "CUDA graph of consecutive steps")
@@ -673,8 +675,8 @@ def run_ours(args):
     chunk = bool(w.chunk)
     if cascade:
         from paged_kv_decode_kf_gb300.step import CascadeStep
-        step = CascadeStep(dev, suffix_splits=args.num_splits, fused_suffix=args.path != "cascade-calls",
-                           out_dtype=out_dtype)
+        step = CascadeStep(dev, prefix_splits=args.prefix_splits, suffix_splits=args.num_splits,
+                           fused_suffix=args.path != "cascade-calls", out_dtype=out_dtype)
         kv_bytes = step.unique_kv_bytes()      # the prefix once, each suffix once
     elif chunk:
         from paged_kv_decode_kf_gb300.step import ChunkStep
