@@ -211,9 +211,12 @@ double model_time(int S, int batch, int num_q_heads, int num_kv_heads, int head_
         t += (rem[i] - done) / rate;
         done = rem[i];
     }
+    // the merge: with one split there is none (the single-launch step writes its
+    // rows directly; a separate merge of one slot is a copy the caller can skip)
     const double rows = (double)batch * num_q_heads;
     const double merge_bytes = rows * (S * (head_dim + 1) * 4.0 * 2.0 + head_dim * 4.0);
-    return t + empties * kEmptyCtaUs / slots + kLaunchUs + merge_bytes / kHbmBytesPerUs + kLaunchUs;
+    const double merge_us = S > 1 ? merge_bytes / kHbmBytesPerUs + kLaunchUs : 0.0;
+    return t + empties * kEmptyCtaUs / slots + kLaunchUs + merge_us;
 }
 
 }  // namespace
