@@ -11,12 +11,13 @@
 // partials of a partition of the tokens equals attention over all of them.
 //
 // Mapping: one warp per (b, h) row, 8 rows per CTA, no block-level
-// synchronisation. Lane k loads lse of partials k, k + 32, ...; a shuffle
-// reduction gives M; each lane turns its lse into a weight, and the weights of
-// 32 partials at a time are broadcast by shuffles while the lanes load the
-// non-empty partials' o rows (16-byte vectors at D = 128, 8 at D = 64), eight
-// partials in flight. An empty partial (lse = -inf) has weight 0 and its o is
-// not read.
+// synchronisation. Lane k loads lse of partials k, k + 32, ... once (kept in
+// registers for up to 64 partials); a shuffle reduction gives M; each lane
+// turns its lse into a weight, and the weights of 32 partials at a time are
+// broadcast by shuffles while the lanes load the non-empty partials' o rows
+// (16-byte vectors at D = 128, 8 at D = 64), sixteen partials in flight: a
+// merge of up to 16 partials is two dependent memory round trips. An empty
+// partial (lse = -inf) has weight 0 and its o is not read.
 #include <math.h>
 
 #include "kf_internal.cuh"
@@ -25,7 +26,7 @@ namespace kf {
 namespace {
 
 constexpr int kRowsPerCta = 8;
-constexpr int kInFlight = 8;  // partials loaded together
+constexpr int kInFlight = 16;  // partials loaded together
 
 template <int D>
 struct MergeVec;
@@ -75,9 +76,11 @@ merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_par
         return;
     }
 
-    // 1. M = max_s lse_s
-    float M = -INFINITY;
-    for (int s = lane; s < S; s += 32) M = fmaxf(M, __ldg(lse_part + (int64_t)s * rows + row));
+    // 1. M = max_s lse_s (the first 64 partials' lse stay in registers)
+    const float l0 = lane < S ? __ldg(lse_part + (int64_t)lane * rows + row) : -INFINITY;
+    const float l1 = lane + 32 < S ? __ldg(lse_part + (int64_t)(lane + 32) * rows + row) : -INFINITY;
+    float M = fmaxf(l0, l1);
+    for (int s = lane + 64; s < S; s += 32) M = fmaxf(M, __ldg(lse_part + (int64_t)s * rows + row));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
 
@@ -87,7 +90,7 @@ merge_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_par
     if (M != -INFINITY) {
         for (int c0 = 0; c0 < S; c0 += 32) {
             const int sl = c0 + lane;
-            const float l = sl < S ? __ldg(lse_part + (int64_t)sl * rows + row) : -INFINITY;
+            const float l = c0 == 0 ? l0 : c0 == 32 ? l1 : (sl < S ? __ldg(lse_part + (int64_t)sl * rows + row) : -INFINITY);
             const float w = l == -INFINITY ? 0.f : expf(l - M);
             wsum += w;
             const int n = S - c0 < 32 ? S - c0 : 32;
