@@ -92,7 +92,7 @@ struct WShape {
 template <int D, int G, int NPW>
 __global__ void __launch_bounds__(NPW == 2 ? 352 : 320, 1)
 mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
-           const __grid_constant__ CUtensorMap tmap_v) {
+           const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_q) {
     using Sh = WShape<D>;
     constexpr int NSL = Sh::kSlots;
     constexpr int KS = D / 16;  // K steps of S = Q K^T
@@ -137,6 +137,7 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_k)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_v)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_q)) : "memory");
         }
         tab_base = ((int64_t)s * p.chunk_blocks * p.block_size) >> bs_shift;
         const int64_t e = tab_base + lane;
@@ -197,7 +198,7 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
             mbar_init(full(i), 1);
             mbar_init(empty(i), 1);
         }
-        mbar_init(q_ready, 256);
+        mbar_init(q_ready, 1);  // the producer's arrival, plus the Q boxes' bytes
         mbar_init(fin, 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(s_full(t), 1);
@@ -220,6 +221,17 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
         // waits for slots and lane k issues the box of the tile's block k.
         const uint32_t box_bytes = (uint32_t)p.block_size * D * 2;
         const int ifirst = warp == Sh::kProducer ? 0 : 1, istep = NPW;
+        if (warp == Sh::kProducer && lane == 0) {
+            // Q first, ahead of the ring's fill: one box per query tile with rows,
+            // (64 d, G heads, 128 / G tokens, D / 64 halves) landing as the tile's
+            // swizzled K-major image (rows = (token, head) pairs). Rows past the
+            // request's queries read the next request's q (or zeros past the
+            // end); their scores are masked and their rows never stored.
+            mbar_arrive_expect_tx(q_ready, (uint32_t)nqt * Sh::kQTileBytes);
+            for (int t = 0; t < nqt; ++t)
+                tma_load_4d(sQ + t * Sh::kQTileBytes, &tmap_q, 0, h * G,
+                            (int)(q0 + (row0 + (int64_t)t * kRowsW) / G), 0, q_ready);
+        }
         int last_k = -1, last_v = -1;  // this warp's last K / V tile issued
         for (int i = ifirst; i < 2 * ntiles; i += istep) {
             const int slot = slot_of(i);
@@ -326,22 +338,6 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     } else if (warp < 8) {
         // ------------------------------- softmax --------------------------------
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        {
-            // q row -> swizzled Q tile tq (K-major, 128-byte rows, 8-row atoms)
-            const uint4 *src = reinterpret_cast<const uint4 *>(p.q + (qrow * Hq + qhead) * D);
-            const uint32_t qb = sQ + tq * Sh::kQTileBytes;
-#pragma unroll
-            for (int c16 = 0; c16 < D / 8; ++c16) {
-                const uint4 v = row_ok ? __ldg(src + c16) : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t a = qb + (c16 >> 3) * Sh::kQHalfBytes + (r >> 3) * 1024 + (r & 7) * 128 +
-                                   (((c16 & 7) ^ (r & 7)) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
-                             "r"(v.w)
-                             : "memory");
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(q_ready);
-        }
         const int64_t lim = row_ok ? (p.causal ? L - C + row / G + 1 : L) : 0;
         const int64_t row_hi = lim < t_hi ? lim : t_hi;  // this row's tokens end here
         const float c = p.scale_log2;
@@ -513,8 +509,25 @@ mqw_kernel(const MqParams p, const __grid_constant__ CUtensorMap tmap_k,
     }
 }
 
+// 4-D view of q [num_q_tokens, Hq, D] bf16: (d % 64, head, token, d / 64), box
+// (64, G, 128 / G, D / 64): one query tile of one KV head's group -- 128 rows of
+// (token, head) pairs, each 64-column half a 16 KiB block of 128-byte rows --
+// landing in the 128-byte-swizzled K-major layout the score MMA reads.
+bool encode_q_map(tc::EncodeFn fn, CUtensorMap *map, const MqParams &p) {
+    const int G = p.num_q_heads / p.num_kv_heads, halves = p.head_dim / 64;
+    const cuuint64_t head = (cuuint64_t)p.head_dim * 2;
+    const cuuint64_t dims[4] = {64, (cuuint64_t)p.num_q_heads, (cuuint64_t)p.num_q_tokens, (cuuint64_t)halves};
+    const cuuint64_t strides[3] = {head, head * p.num_q_heads, 128};
+    const cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)(kRowsW / G), (cuuint32_t)halves};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t *>(p.q), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int G, int NPW>
-cudaError_t launch_w(const MqParams &p, cudaStream_t stream, const CUtensorMap &mk, const CUtensorMap &mv) {
+cudaError_t launch_w(const MqParams &p, cudaStream_t stream, const CUtensorMap &mk, const CUtensorMap &mv,
+                         const CUtensorMap &mq) {
     using Sh = WShape<D>;
     static std::atomic<uint64_t> done{0};
     int dev = 0;
@@ -528,26 +541,28 @@ cudaError_t launch_w(const MqParams &p, cudaStream_t stream, const CUtensorMap &
         done.fetch_or(bit);
     }
     const dim3 grid(p.num_splits, p.num_kv_heads, p.batch * p.q_tiles);
-    mqw_kernel<D, G, NPW><<<grid, Sh::threads(NPW), Sh::kSmemBytes, stream>>>(p, mk, mv);
+    mqw_kernel<D, G, NPW><<<grid, Sh::threads(NPW), Sh::kSmemBytes, stream>>>(p, mk, mv, mq);
     return cudaGetLastError();
 }
 
 // Two producer warps by default; KF_MQW_PRODUCERS = 1 selects one (read per
 // call, for comparisons).
 template <int D, int G>
-cudaError_t launch_w(const MqParams &p, cudaStream_t stream, const CUtensorMap &mk, const CUtensorMap &mv) {
+cudaError_t launch_w(const MqParams &p, cudaStream_t stream, const CUtensorMap &mk, const CUtensorMap &mv,
+                         const CUtensorMap &mq) {
     const char *s = getenv("KF_MQW_PRODUCERS");
-    if (s && strcmp(s, "1") == 0) return launch_w<D, G, 1>(p, stream, mk, mv);
-    return launch_w<D, G, 2>(p, stream, mk, mv);
+    if (s && strcmp(s, "1") == 0) return launch_w<D, G, 1>(p, stream, mk, mv, mq);
+    return launch_w<D, G, 2>(p, stream, mk, mv, mq);
 }
 
 template <int D>
-cudaError_t launch_w_g(const MqParams &p, cudaStream_t stream, const CUtensorMap &mk, const CUtensorMap &mv) {
+cudaError_t launch_w_g(const MqParams &p, cudaStream_t stream, const CUtensorMap &mk, const CUtensorMap &mv,
+                         const CUtensorMap &mq) {
     switch (p.num_q_heads / p.num_kv_heads) {
-        case 1: return launch_w<D, 1>(p, stream, mk, mv);
-        case 2: return launch_w<D, 2>(p, stream, mk, mv);
-        case 4: return launch_w<D, 4>(p, stream, mk, mv);
-        case 8: return launch_w<D, 8>(p, stream, mk, mv);
+        case 1: return launch_w<D, 1>(p, stream, mk, mv, mq);
+        case 2: return launch_w<D, 2>(p, stream, mk, mv, mq);
+        case 4: return launch_w<D, 4>(p, stream, mk, mv, mq);
+        case 8: return launch_w<D, 8>(p, stream, mk, mv, mq);
     }
     return cudaErrorInvalidValue;
 }
@@ -563,9 +578,11 @@ cudaError_t launch_multiquery_tc05w(MqParams p, cudaStream_t stream, void *encod
     if ((int64_t)p.batch * p.q_tiles > 65535) return cudaErrorInvalidValue;
     tc::EncodeFn fn = reinterpret_cast<tc::EncodeFn>(encode);
     CUtensorMap mk, mv;
-    if (!encode_block_map(fn, &mk, p.k_cache, p) || !encode_block_map(fn, &mv, p.v_cache, p))
+    CUtensorMap mq;
+    if (!encode_block_map(fn, &mk, p.k_cache, p) || !encode_block_map(fn, &mv, p.v_cache, p) ||
+        !encode_q_map(fn, &mq, p))
         return cudaErrorInvalidValue;
-    return p.head_dim == 128 ? launch_w_g<128>(p, stream, mk, mv) : launch_w_g<64>(p, stream, mk, mv);
+    return p.head_dim == 128 ? launch_w_g<128>(p, stream, mk, mv, mq) : launch_w_g<64>(p, stream, mk, mv, mq);
 }
 
 }  // namespace kf
