@@ -12,9 +12,12 @@ configuration: the ragged continuous batch (256 requests, 70/25/5 % of them
 KV-read GB/s over all ranks: algorithmic KV bytes (sum_b L_b * 2 * Hkv * D *
 2) per step divided by the device time of a step, inputs resident in HBM,
 timed with CUDA events between a barrier and a synchronize on both sides, max
-over ranks. `e2e` is the same metric with the step's inputs copied from pinned
-host memory and its result copied back inside the timed region, with the
-split of its time into copies, device step and host launch/wait.
+over ranks. `e2e` is the same metric through the C ABI with host buffers,
+host waiting for each step's result: for the single-launch step, the step
+kernel reads its per-step inputs from pinned host memory and writes out and
+lse there (zero-copy), and `e2e_copies` is the copy-based run; for the other
+paths, one H2D copy of the inputs and one D2H copy of the result per step.
+Each carries the split of its time into device step and host launch/wait.
 `per_config` (one GPU, default workload) times every decode configuration
 (tiny, llama8b, longctx, shard4, ragged): per-step median / p10 / p90 over
 at least 50 graph-replayed steps, KV GB/s and its fraction of the measured
@@ -465,12 +468,12 @@ def percentile(xs, q: float) -> float:
     return ys[lo] + (ys[hi] - ys[lo]) * (pos - lo)
 
 
-def step_distribution(step, min_samples: int = 50, target_s: float = 0.25):
+def step_distribution(step, min_samples: int = 50, target_s: float = 0.3):
     """Per-step device times (ms) of `step` replayed from CUDA graphs.
 
     A sample is one graph replay of g consecutive steps divided by g, with g
-    the smallest count that makes a sample at least 200 us (g = 1 for every
-    step that long on its own, so most samples are single steps). The stream
+    the smallest count that makes a sample at least 1 ms (g = 1 for a step that
+    long on its own), so a replay's own launch cost weighs little. The stream
     first sleeps while the host enqueues every replay and event, so the events
     see device time, not host launch gaps. Returns (samples, g, the wall-clock
     window of the loop)."""
@@ -485,7 +488,7 @@ def step_distribution(step, min_samples: int = 50, target_s: float = 0.25):
     b.record()
     torch.cuda.synchronize()
     est_ms = max(a.elapsed_time(b) / 10, 1e-3)
-    g = max(1, int(math.ceil(0.2 / est_ms)))
+    g = max(1, int(math.ceil(1.0 / est_ms)))
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         for _ in range(g):
@@ -639,6 +642,94 @@ def e2e_breakdown(e2e_step, graph, body, stage_dev, stage_host, res_dev, res_hos
     return {"h2d_us": h2d, "step_us": dev_step, "d2h_us": d2h, "device_span_us": span,
             "host_launch_call_us": statistics.median(launches),
             "host_launch_latency_and_wait_us": wall_s * 1e6 - span}
+
+
+def zero_copy_e2e(step, K: int, world: int, kv_bytes: int, barrier, use_graph: bool):
+    """End to end through kf_decode_step with the step's per-step inputs (q,
+    k_new, v_new, context lengths, block tables) and its result (out, lse) in
+    pinned host memory, which the step kernel reads and writes in place over
+    the CPU-GPU link (CUDA unified addressing): no copy launches, the bytes
+    still cross the link every step. Each step is one launch (a CUDA graph of
+    the call) and the host's wait for the result. Returns the e2e record, with
+    whether the result equals the device-buffer step's bit for bit."""
+    import copy
+    import torch
+    from paged_kv_decode_kf_gb300.step import DecodeStep
+
+    inp = copy.copy(step.inp)
+    h2d = 0
+    for n in ("q", "k_new", "v_new", "ctx_before", "block_tables"):
+        t = getattr(inp, n).cpu().pin_memory()
+        setattr(inp, n, t)
+        h2d += t.numel() * t.element_size()
+    zs = DecodeStep(inp, num_splits=step.num_splits, fused=True, out_dtype=step.out.dtype)
+    zs.out = torch.empty(zs.out.shape, dtype=zs.out.dtype).pin_memory()
+    zs.lse = torch.empty(zs.lse.shape, dtype=torch.float32).pin_memory()
+    d2h = zs.out.numel() * zs.out.element_size() + zs.lse.numel() * 4
+
+    zs.run()
+    torch.cuda.synchronize()
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            zs.run()
+
+    def launch():
+        if graph is not None:
+            graph.replay()
+        else:
+            zs.run()
+
+    def one():
+        launch()
+        torch.cuda.synchronize()
+
+    Ke = max(3, min(K, 400))
+    for _ in range(3):
+        one()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(Ke):
+        one()
+    te = (time.perf_counter() - t0) / Ke
+    barrier()
+    te = max_over_ranks(te)
+
+    step.run()                      # the same step with device buffers
+    torch.cuda.synchronize()
+    same = bool(torch.equal(zs.out, step.out.cpu()) and torch.equal(zs.lse, step.lse.cpu()))
+
+    def timed(fn, reps=20):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(10_000_000)
+        for a, b in evs:
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+
+    launches = []
+    for _ in range(50):
+        t = time.perf_counter()
+        launch()
+        launches.append((time.perf_counter() - t) * 1e6)
+        torch.cuda.synchronize()
+    step_us = timed(zs.run)
+    return {"value": whole_job_gbs(kv_bytes, world, te), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": te * 1e3, "steps": Ke,
+            "out_dtype": "bf16" if zs.out.dtype == torch.bfloat16 else "f32",
+            "copies_per_step": "none: the step kernel reads q, k_new, v_new, context lengths and block "
+                               "tables from pinned host memory and writes out and lse there (zero-copy)",
+            "launch": ("one CUDA graph of the kf_decode_step call per step" if graph is not None
+                       else "one kf_decode_step call per step") + ", host waits for the result",
+            "result_equals_device_buffer_step": same,
+            "breakdown": {"step_us": step_us, "step_with_device_buffers_us": timed(step.run),
+                          "host_launch_call_us": statistics.median(launches),
+                          "host_launch_latency_and_wait_us": te * 1e6 - step_us}}
 
 
 def run_ours(args):
@@ -810,7 +901,7 @@ def run_ours(args):
     # one device staging buffer with a pinned host twin, so one H2D copy per
     # step refreshes them all; out and lse share one buffer read back by one
     # D2H copy.
-    e2e = None
+    e2e, e2e_copies = None, None
     if not args.no_e2e:
         names = ["q", "k_new", "v_new", "ctx_before", "ctx_after", "block_tables"]
         for extra in ("prefix_table", "suffix_tables", "suffix_ctx_before", "suffix_ctx_after", "q_chunk",
@@ -900,6 +991,11 @@ def run_ours(args):
                if e2e_graph is not None else "host launches, host waits for the result",
                "breakdown": e2e_breakdown(e2e_step, e2e_graph, e2e_body, stage_dev, stage_host, res_dev, res_host,
                                           step_e, te)}
+        if step.fused:
+            # the single-launch step also takes its per-step tensors in pinned
+            # host memory: the headline e2e, the copy-based run kept beside it
+            e2e_copies = e2e
+            e2e = zero_copy_e2e(step, K, world, kv_bytes, barrier, not args.no_graph)
 
     peak, peak_src = hbm_peak()
     per_config, windows = None, []
@@ -1017,6 +1113,7 @@ def run_ours(args):
                        "parallelism": "replica per GPU" if world > 1 else "1 GPU"},
             "roofline": roofline,
             "e2e": e2e,
+            "e2e_copies": e2e_copies,
             "cpu_baseline": cpu,
             "per_config": per_config,
             "clocks": clk,

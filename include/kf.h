@@ -27,7 +27,14 @@
  * Conventions for every call:
  *  - Memory: every pointer is DEVICE memory owned by the caller, 16-byte
  *    aligned, densely packed in the layout stated. The library never
- *    allocates per call and keeps no per-call state.
+ *    allocates per call and keeps no per-call state. One exception: the
+ *    kf_decode_step calls (all four) also take pinned host memory that the GPU
+ *    addresses directly (CUDA unified addressing, e.g. cudaHostAlloc) for
+ *    their per-step inputs and outputs -- q, k_new, v_new, block_tables,
+ *    context_lens_before, out and lse_out -- and read or write it in place over
+ *    the host link; on GB300 (NVLink-C2C) that is faster for a step's small
+ *    inputs and outputs than copying them. The caches, scales, workspace and
+ *    extra partials stay device memory.
  *  - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL = legacy
  *    default stream) and the call returns without synchronising.
  *  - Host errors: arguments that can be checked on the host are checked

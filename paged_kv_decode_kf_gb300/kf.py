@@ -116,6 +116,18 @@ def _dev(t: torch.Tensor, dtype, name: str) -> int:
     return t.data_ptr()
 
 
+def _io(t: torch.Tensor, dtype, name: str) -> int:
+    """A per-step input or output of the kf_decode_step calls: a CUDA tensor, or
+    a pinned host tensor the GPU reads or writes in place (zero-copy)."""
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError("%s must be a CUDA tensor or pinned host memory" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
 def kf_version() -> int:
     return _lib.kf_version()
 
@@ -250,27 +262,29 @@ def kf_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_
                    workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                    out_dtype=torch.float32, lse_out: Optional[torch.Tensor] = None, want_lse: bool = True,
                    stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """Append + split attention + merge in one launch; returns (out, lse)."""
+    """Append + split attention + merge in one launch; returns (out, lse).
+    q, k_new, v_new, block_tables, context_lens_before, out and lse_out may be
+    pinned host tensors (read and written by the kernel in place)."""
     B, hq, d = q.shape
     nb, bs, hkv, d2 = k_cache.shape
     if out is None:
-        out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
+        out = torch.empty((B, hq, d), dtype=out_dtype, device=k_cache.device)
     code = {torch.float32: KF_F32, torch.bfloat16: KF_BF16}.get(out.dtype)
     if code is None:
         raise ValueError("out must be float32 or bfloat16")
     if lse_out is None and want_lse:
-        lse_out = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+        lse_out = torch.empty((B, hq), dtype=torch.float32, device=k_cache.device)
     if workspace is None and num_splits != 1:
         raise ValueError("num_splits > 1 and the balanced schedule need a workspace (make_workspace)")
     ws_ptr = None if workspace is None else _dev(workspace, torch.uint8, "workspace")
     ws_bytes = 0 if workspace is None else workspace.numel()
     _check(_lib.kf_decode_step(
-        _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _io(q, torch.bfloat16, "q"), _io(k_new, torch.bfloat16, "k_new"), _io(v_new, torch.bfloat16, "v_new"),
         _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
-        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
-        _dev(context_lens_before, torch.int32, "context_lens_before"), int(max_context_len), B, hq, hkv, d,
-        bs, nb, float(scale), int(num_splits), ws_ptr, ws_bytes, _dev(out, out.dtype, "out"), code,
-        None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
+        _io(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _io(context_lens_before, torch.int32, "context_lens_before"), int(max_context_len), B, hq, hkv, d,
+        bs, nb, float(scale), int(num_splits), ws_ptr, ws_bytes, _io(out, out.dtype, "out"), code,
+        None if lse_out is None else _io(lse_out, torch.float32, "lse_out"), _stream(stream)),
         "kf_decode_step")
     return out, lse_out
 
@@ -291,21 +305,21 @@ def kf_decode_step_merge_partials(q: torch.Tensor, k_new: torch.Tensor, v_new: t
     if tuple(extra_out_partial.shape) != (n_ex, B, hq, d) or tuple(extra_lse_partial.shape) != (n_ex, B, hq):
         raise ValueError("extra partials must be [n, B, Hq, D] and [n, B, Hq]")
     if out is None:
-        out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
+        out = torch.empty((B, hq, d), dtype=out_dtype, device=k_cache.device)
     code = {torch.float32: KF_F32, torch.bfloat16: KF_BF16}.get(out.dtype)
     if code is None:
         raise ValueError("out must be float32 or bfloat16")
     if lse_out is None and want_lse:
-        lse_out = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+        lse_out = torch.empty((B, hq), dtype=torch.float32, device=k_cache.device)
     _check(_lib.kf_decode_step_merge_partials(
-        _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _io(q, torch.bfloat16, "q"), _io(k_new, torch.bfloat16, "k_new"), _io(v_new, torch.bfloat16, "v_new"),
         _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
-        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
-        _dev(context_lens_before, torch.int32, "context_lens_before"), int(max_context_len), B, hq, hkv, d,
+        _io(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _io(context_lens_before, torch.int32, "context_lens_before"), int(max_context_len), B, hq, hkv, d,
         bs, nb, float(scale), int(num_splits), _dev(extra_out_partial, torch.float32, "extra_out_partial"),
         _dev(extra_lse_partial, torch.float32, "extra_lse_partial"), n_ex,
-        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _dev(out, out.dtype, "out"), code,
-        None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _io(out, out.dtype, "out"), code,
+        None if lse_out is None else _io(lse_out, torch.float32, "lse_out"), _stream(stream)),
         "kf_decode_step_merge_partials")
     return out, lse_out
 
@@ -324,12 +338,12 @@ def kf_decode_step_static(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Ten
     if code is None:
         raise ValueError("out must be float32 or bfloat16")
     _check(_lib.kf_decode_step_static(
-        _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _io(q, torch.bfloat16, "q"), _io(k_new, torch.bfloat16, "k_new"), _io(v_new, torch.bfloat16, "v_new"),
         _dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
-        _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
-        _dev(context_lens_before, torch.int32, "context_lens_before"), int(max_context_len), B, hq, hkv, d,
-        bs, nb, float(scale), int(num_splits), _dev(out, out.dtype, "out"), code,
-        None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
+        _io(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+        _io(context_lens_before, torch.int32, "context_lens_before"), int(max_context_len), B, hq, hkv, d,
+        bs, nb, float(scale), int(num_splits), _io(out, out.dtype, "out"), code,
+        None if lse_out is None else _io(lse_out, torch.float32, "lse_out"), _stream(stream)),
         "kf_decode_step_static")
 
 
@@ -379,27 +393,28 @@ def kf_decode_step_fp8(q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, bloc
                        context_lens_before, max_context_len: int, scale: float, num_splits: int,
                        workspace=None, out=None, out_dtype=torch.float32, lse_out=None, want_lse=True,
                        stream=None):
-    """Single-launch decode step over E4M3 caches; returns (out, lse)."""
+    """Single-launch decode step over E4M3 caches; returns (out, lse). The
+    per-step tensors may be pinned host memory, as for kf_decode_step."""
     B, hq, d = q.shape
     nb, bs, hkv, d2 = k_cache.shape
     if out is None:
-        out = torch.empty((B, hq, d), dtype=out_dtype, device=q.device)
+        out = torch.empty((B, hq, d), dtype=out_dtype, device=k_cache.device)
     code = {torch.float32: KF_F32, torch.bfloat16: KF_BF16}.get(out.dtype)
     if code is None:
         raise ValueError("out must be float32 or bfloat16")
     if lse_out is None and want_lse:
-        lse_out = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+        lse_out = torch.empty((B, hq), dtype=torch.float32, device=k_cache.device)
     if workspace is None and num_splits != 1:
         raise ValueError("num_splits > 1 and the balanced schedule need a workspace (make_workspace)")
     _check(_lib.kf_decode_step_fp8(
-        _dev(q, torch.bfloat16, "q"), _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+        _io(q, torch.bfloat16, "q"), _io(k_new, torch.bfloat16, "k_new"), _io(v_new, torch.bfloat16, "v_new"),
         _dev8(k_cache, "k_cache"), _dev8(v_cache, "v_cache"), _dev(k_scale, torch.float32, "k_scale"),
-        _dev(v_scale, torch.float32, "v_scale"), _dev(block_tables, torch.int32, "block_tables"),
-        block_tables.shape[1], _dev(context_lens_before, torch.int32, "context_lens_before"),
+        _dev(v_scale, torch.float32, "v_scale"), _io(block_tables, torch.int32, "block_tables"),
+        block_tables.shape[1], _io(context_lens_before, torch.int32, "context_lens_before"),
         int(max_context_len), B, hq, hkv, d, bs, nb, float(scale), int(num_splits),
         None if workspace is None else _dev(workspace, torch.uint8, "workspace"),
-        0 if workspace is None else workspace.numel(), _dev(out, out.dtype, "out"), code,
-        None if lse_out is None else _dev(lse_out, torch.float32, "lse_out"), _stream(stream)),
+        0 if workspace is None else workspace.numel(), _io(out, out.dtype, "out"), code,
+        None if lse_out is None else _io(lse_out, torch.float32, "lse_out"), _stream(stream)),
         "kf_decode_step_fp8")
     return out, lse_out
 

@@ -33,7 +33,7 @@ class DecodeStep:
             raise ValueError("the single-launch step covers unsharded workloads with the append")
         self.fused = fused
         B, Hq, D = w.batch, w.num_q_heads, w.head_dim
-        dev = inp.q.device
+        dev = inp.k_cache.device
         # host-side bounds, computed once: reading them per step would synchronise
         self.max_ctx = inp.max_ctx_after
         if w.shards:

@@ -185,3 +185,57 @@ def test_graph_captured_step_matches_eager(kind):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(step.out, ref_o) and torch.equal(step.lse, ref_l)
+
+
+@pytest.mark.parametrize("kind", ["splits", "balanced", "static", "merge_partials", "fp8"])
+def test_pinned_host_step_io(kind, kf):
+    """The step calls read q, k_new, v_new, block tables and context lengths
+    from pinned host memory and write out and lse there (zero-copy): the result
+    equals the device-buffer call's bit for bit and matches the oracle."""
+    lens = (500, 31, 2000, 64, 1, 777)
+    w = wl.scaled(wl.CONFIGS["ragged"], batch=len(lens), lengths=wl.Fixed(lens), spare_blocks=3)
+    if kind == "fp8":
+        w = wl.with_kv_dtype(w, "fp8")
+    dev = wl.make_inputs(w, "cuda")
+    hv = None if kind == "fp8" else HostView(dev, range(w.batch))
+    S = kf.KF_SPLITS_BALANCED if kind == "balanced" else 5
+    pin = lambda t: t.cpu().pin_memory()
+    h = {n: pin(getattr(dev, n)) for n in ("q", "k_new", "v_new", "block_tables", "ctx_before")}
+    shape = (w.batch, w.num_q_heads, w.head_dim)
+    ws = None if kind == "static" else kf.make_workspace(w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, S)
+    n_ex = 2
+    ex_o = torch.randn((n_ex,) + shape, device="cuda") if kind == "merge_partials" else None
+    ex_l = torch.randn((n_ex, w.batch, w.num_q_heads), device="cuda") if kind == "merge_partials" else None
+
+    def call(src, out, lse):
+        args = (src["q"], src["k_new"], src["v_new"], dev.k_cache, dev.v_cache)
+        rest = (src["block_tables"], src["ctx_before"], dev.max_ctx_after, w.scale, S)
+        if kind == "static":
+            kf.kf_decode_step_static(*args, *rest, out, lse_out=lse)
+        elif kind == "merge_partials":
+            kf.kf_decode_step_merge_partials(*args, *rest, ex_o, ex_l, ws, out=out, lse_out=lse)
+        elif kind == "fp8":
+            kf.kf_decode_step_fp8(*args, dev.k_scale, dev.v_scale, *rest, ws, out=out, lse_out=lse)
+        else:
+            kf.kf_decode_step(*args, *rest, ws, out=out, lse_out=lse)
+
+    d = {n: getattr(dev, n) for n in h}
+    out_d = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    lse_d = torch.empty(shape[:2], dtype=torch.float32, device="cuda")
+    call(d, out_d, lse_d)
+    out_h = torch.full(shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.full(shape[:2], float("nan"), dtype=torch.float32).pin_memory()
+    call(h, out_h, lse_h)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, out_d.cpu()) and torch.equal(lse_h, lse_d.cpu())
+    if kind in ("merge_partials", "fp8"):
+        return          # their numerics are checked against the oracle in their own tests
+    _check_against_oracle(dev, hv, out_h, lse_h, what="pinned host I/O, %s" % kind)
+
+
+def test_pageable_host_tensor_refused(kf):
+    w = wl.scaled(wl.CONFIGS["tiny"], batch=2, lengths=wl.Fixed((20, 40)))
+    dev = wl.make_inputs(w, "cuda")
+    with pytest.raises(ValueError, match="pinned"):
+        kf.kf_decode_step(dev.q.cpu(), dev.k_new, dev.v_new, dev.k_cache, dev.v_cache, dev.block_tables,
+                          dev.ctx_before, dev.max_ctx_after, w.scale, 1)
