@@ -702,6 +702,45 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
     const int Hq = p.num_q_heads;
     const bool report = threadIdx.x == 0 && s == 0 && hg == 0;
 
+    // Loads that do not depend on the context length go out first, so that
+    // their latencies overlap that of the length: the producer's first 32 table
+    // entries (a split starts at logical block s * chunk_blocks), the
+    // consumers' query rows and, for FP8 caches, their KV head's scales.
+    int64_t tab_base = -1;
+    int32_t tab_ent = -1;
+    const int g = lane >> 2;
+    const int qd = lane & 3;
+    const int hkv = h0 + (warp < HPC ? warp : 0);
+    const int hq = hkv * G;  // first query head of a consumer warp's KV head
+    uint32_t qb[KS][2];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qb[ks][1] = 0u;
+    float k_sc = 1.f, v_sc = 1.f;
+    if (warp == HPC) {
+        tab_base = (int64_t)s * p.chunk_blocks;
+        const int64_t e = tab_base + lane;
+        tab_ent = e < p.bt_stride ? p.block_tables[(int64_t)b * p.bt_stride + e] : -1;
+    } else {
+        if (g < G) {
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + ((int64_t)b * Hq + hq + g) * D);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                if (KV8) {
+                    const uint2 v = reinterpret_cast<const uint2 *>(qrow)[4 * ks + qd];
+                    qb[ks][0] = v.x;
+                    qb[ks][1] = v.y;
+                } else {
+                    qb[ks][0] = qrow[8 * ks + qd];
+                    qb[ks][1] = qrow[8 * ks + 4 + qd];
+                }
+            }
+        }
+        if (KV8) {
+            k_sc = p.k_scale[hkv];
+            v_sc = p.v_scale[hkv];
+        }
+    }
+
     // token range of this split; in the fused step the range covers the new token too
     int64_t p_new = -1;  // position the step appends (fused only)
     int n_ne = 0;
@@ -750,8 +789,6 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
         // coalesced load, lane e holds logical block base + e), so a TMA issue
         // never waits on a dependent load; lane 0 waits for slots and issues.
         const int bs_shift = block_shift(p.block_size);
-        int64_t tab_base = -1;
-        int32_t tab_ent = -1;
         for (int i = 0; i < n_sub; ++i) {
             const int st = i % NS;
             int go = 1;
@@ -788,30 +825,9 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
         if (!FUSED) return;
     } else {
         // ------------------------------- consumers --------------------------------
-        const int g = lane >> 2;
-        const int qd = lane & 3;
-        const int hkv = h0 + warp;
-        const int hq = hkv * G;  // first query head of this warp's KV head
-
-        // Q^T as B fragments, as load_q_raw + prep_q build them (written out here:
-        // as calls the FP8 instantiation with three CTAs per SM spills a register)
-        uint32_t qb[KS][2];
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) qb[ks][0] = qb[ks][1] = 0u;
-        if (g < G) {
-            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + ((int64_t)b * Hq + hq + g) * D);
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                if (KV8) {
-                    const uint2 v = reinterpret_cast<const uint2 *>(qrow)[4 * ks + qd];
-                    qb[ks][0] = v.x;
-                    qb[ks][1] = v.y;
-                } else {
-                    qb[ks][0] = qrow[8 * ks + qd];
-                    qb[ks][1] = qrow[8 * ks + 4 + qd];
-                }
-            }
-        }
+        // Q^T as B fragments (loaded above as load_q_raw does; prep_q's scaling
+        // written out here: as calls the FP8 instantiation with three CTAs per SM
+        // spills a register)
         // FP8 cache: the products run in fp16. q (bf16, 8 significant bits) goes to
         // fp16 exactly after an exact power-of-two scaling 2^qe that puts the
         // warp's largest |q| in [2^14, 2^15); 2^-qe goes into the score scale
@@ -834,8 +850,8 @@ decode_tc_kernel(const DecodeParams p, const StepParams sp, const __grid_constan
             }
         }
         // per-head dequantisation scales of an FP8 cache
-        const float sl2 = KV8 ? p.scale_log2 * p.k_scale[hkv] * qe_scale : p.scale_log2;
-        const float vsc = KV8 ? p.v_scale[hkv] : 1.f;
+        const float sl2 = KV8 ? p.scale_log2 * k_sc * qe_scale : p.scale_log2;
+        const float vsc = KV8 ? v_sc : 1.f;
 
         float oacc[KS][4];
 #pragma unroll
