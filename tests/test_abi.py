@@ -135,6 +135,19 @@ def test_binding_rejects_host_tensors(kf):
                                      out_partial=torch.zeros(1), lse_partial=torch.zeros(1))
 
 
+def test_step_binding_refuses_pageable_host_tensors(kf):
+    """The step calls take pinned host tensors for their per-step inputs and
+    outputs (read in place by the kernel); pageable host memory is refused
+    before any call."""
+    import torch
+    q = torch.zeros(2, 8, 128, dtype=torch.bfloat16)
+    cache = torch.zeros(4, 16, 2, 128, dtype=torch.bfloat16)
+    for call in (kf.kf_decode_step, kf.kf_decode_step_static):
+        with pytest.raises(ValueError, match="pinned"):
+            call(q, q[:, :2], q[:, :2], cache, cache, torch.zeros(2, 2, dtype=torch.int32),
+                 torch.ones(2, dtype=torch.int32), 4, 0.1, 1, out=torch.zeros(2, 8, 128))
+
+
 def test_decode_step_host_checks(kf):
     lib = kf.raw()
     need = kf.kf_decode_step_workspace_size(4, 32, 8, 128, 10)
