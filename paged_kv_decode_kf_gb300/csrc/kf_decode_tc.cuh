@@ -46,10 +46,12 @@
 // ldmatrix as is; each thread's 32-bit register then holds 4 consecutive
 // codes of one token, widened with cvt.rn.f16x2.e4m3x2 and used as the A
 // fragment of S^T = K Q^T under the k <-> d order (2qd+e <-> 4qd+e,
-// 2qd+8+e <-> 4qd+2+e), with Q^T's fragments loaded in the same order. V's
-// widened pairs form 8x8 tiles (rows tokens) that movmatrix.trans turns into
-// the A fragment of O^T += V^T P^T with O's rows in a permuted d order,
-// undone when the rows are written; P enters that product as one fp16 value
+// 2qd+8+e <-> 4qd+2+e), with Q^T's fragments loaded in the same order. V goes
+// through a transposed byte ldmatrix (16 x 16 codes per tile): each thread
+// gets one d of 4 consecutive tokens, whose widened pairs are the A fragment
+// of O^T += V^T P^T directly, under a permuted token order (k 2qd+e <-> token
+// 4qd+e, 2qd+8+e <-> 4qd+2+e) that the S^T rows -- K's ldmatrix row addresses
+// -- and so P^T follow; P enters that product as one fp16 value
 // (11 significant bits against bf16's 8, so no P_lo term). The scales
 // multiply the scores and the output. The fused step quantises the appended
 // row (x / scale, nearest-even, saturating) with cvt.rn.satfinite.e4m3x2.f32.
@@ -144,6 +146,22 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
+}
+
+// Two 16x16 tiles of bytes, transposed: lanes 0-15 / 16-31 give the 16 row
+// addresses of tile 0 / 1; lane 4g + q receives, of tile i, rows 4q .. 4q+3 of
+// column g in r[2i] and of column g + 8 in r[2i+1] (byte j = row 4q + j).
+__device__ __forceinline__ void ldsm_b8_x2_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// FP8 stages take the 16 tokens of a stage in the order that a transposed byte
+// ldmatrix of V delivers them: MMA k index (and S^T row) 2q + j is token
+// 4q + j, and 2q + 8 + j is token 4q + 2 + j (q < 4, j < 2).
+__device__ __forceinline__ int fp8_token(int r) {
+    return r < 8 ? 4 * (r >> 1) + (r & 1) : 4 * ((r - 8) >> 1) + 2 + (r & 1);
 }
 
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
@@ -504,9 +522,10 @@ __device__ __forceinline__ void stage_math(uint32_t kbuf, uint32_t vbuf, int nva
         // one ldmatrix.x4 = 16 tokens x 32 d codes; each 32-bit register holds 4
         // consecutive codes of one token, widened to the A fragment of k-step
         // (low pair -> k 2qd..+1, high pair -> k 2qd+8..+9)
+        // (S^T row r is token fp8_token(r), the order V's fragments arrive in)
+        const int t = fp8_token(lr + ((lj & 1) << 3));
 #pragma unroll
         for (int kk = 0; kk < KS / 2; ++kk) {
-            const int t = lr + ((lj & 1) << 3);
             const int chunk = 2 * kk + (lj >> 1);
             uint32_t fr[4];
             ldsm_x4(kbuf + swz<RB>(t, chunk), fr);
@@ -531,11 +550,13 @@ __device__ __forceinline__ void stage_math(uint32_t kbuf, uint32_t vbuf, int nva
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) sc[e] += sd[e];
-    // scores in base 2, masked past the end; sc[0..1] token g, sc[2..3] token g+8
-    const float x0 = g < nvalid ? sc[0] * sl2 : -INFINITY;
-    const float x1 = g < nvalid ? sc[1] * sl2 : -INFINITY;
-    const float x2 = g + 8 < nvalid ? sc[2] * sl2 : -INFINITY;
-    const float x3 = g + 8 < nvalid ? sc[3] * sl2 : -INFINITY;
+    // scores in base 2, masked past the end; sc[0..1] row g, sc[2..3] row g+8
+    // (tokens g, g + 8; FP8: fp8_token of them)
+    const int tok0 = KV8 ? fp8_token(g) : g, tok1 = KV8 ? fp8_token(g + 8) : g + 8;
+    const float x0 = tok0 < nvalid ? sc[0] * sl2 : -INFINITY;
+    const float x1 = tok0 < nvalid ? sc[1] * sl2 : -INFINITY;
+    const float x2 = tok1 < nvalid ? sc[2] * sl2 : -INFINITY;
+    const float x3 = tok1 < nvalid ? sc[3] * sl2 : -INFINITY;
     float mx[2] = {fmaxf(x0, x2), fmaxf(x1, x3)};
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -578,22 +599,19 @@ __device__ __forceinline__ void stage_math(uint32_t kbuf, uint32_t vbuf, int nva
 
     // O^T += V^T P^T : rows = d, cols = query heads
     if (KV8) {
-        // V codes: the widened pairs of one token form 8x8 fp16 tiles (rows =
-        // tokens, cols = d 4qd+{0,1} or 4qd+{2,3}); movmatrix.trans turns them into
-        // A fragments whose rows are d in that permuted order
+        // V codes through a transposed byte ldmatrix, two 16-d tiles at a time:
+        // this lane gets d = g and g + 8 of tokens 4qd .. 4qd+3, whose widened
+        // pairs are the A fragment of O^T (rows d in order) at k 2qd.. / 2qd+8..
+        // under the token order of fp8_token
 #pragma unroll
         for (int mm = 0; mm < KS / 2; ++mm) {
-            const int t = lr + ((lj & 1) << 3);
-            const int chunk = 2 * mm + (lj >> 1);
             uint32_t fr[4];
-            ldsm_x4(vbuf + swz<RB>(t, chunk), fr);
+            ldsm_b8_x2_trans(vbuf + swz<RB>(lane & 15, 2 * mm + (lane >> 4)), fr);
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 const uint32_t ra = fr[2 * h2], rb = fr[2 * h2 + 1];
-                const uint32_t af[4] = {movmatrix_trans(e4m3x2_to_f16x2(ra)),
-                                        movmatrix_trans(e4m3x2_to_f16x2(ra >> 16)),
-                                        movmatrix_trans(e4m3x2_to_f16x2(rb)),
-                                        movmatrix_trans(e4m3x2_to_f16x2(rb >> 16))};
+                const uint32_t af[4] = {e4m3x2_to_f16x2(ra), e4m3x2_to_f16x2(rb), e4m3x2_to_f16x2(ra >> 16),
+                                        e4m3x2_to_f16x2(rb >> 16)};
                 mma_f16(oacc[2 * mm + h2], af, bh0, bh1);
             }
         }
@@ -633,10 +651,9 @@ __device__ __forceinline__ void write_rows(const float (&oacc)[D / 16][4], float
     const float lse1 = (m_run[1] + log2f(l_acc[1])) * 0.6931471805599453f;
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
-        // rows of O^T held by this thread: bf16 path d = 16mt+g and +8; FP8 path
-        // (permuted rows) d = 16mt + 4(g/2) + g%2 and +2
-        const int d0 = KV8 ? 16 * mt + 4 * (g >> 1) + (g & 1) : 16 * mt + g;
-        const int d1 = KV8 ? d0 + 2 : d0 + 8;
+        // rows of O^T held by this thread: d = 16mt + g and + 8
+        const int d0 = 16 * mt + g;
+        const int d1 = d0 + 8;
         const float v00 = oacc[mt][0] * inv0, v01 = oacc[mt][2] * inv0;
         const float v10 = oacc[mt][1] * inv1, v11 = oacc[mt][3] * inv1;
         if (o_dst != nullptr) {
