@@ -56,10 +56,12 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="ragged")
     ap.add_argument("--decode-kernel", default="tc", choices=["tc", "simt"])
-    ap.add_argument("--path", default="auto", choices=["auto", "fused", "calls", "cascade", "cascade-calls"],
+    ap.add_argument("--path", default="auto",
+                    choices=["auto", "fused", "calls", "cascade", "cascade-serial", "cascade-calls"],
                     help="fused: kf_decode_step (one launch); calls: append, attention, merge; "
-                         "cascade (shared-prefix workloads): prefix pass + kf_decode_step_merge_partials; "
-                         "cascade-calls: append, prefix pass, suffix decode, merge; "
+                         "cascade (shared-prefix workloads): prefix pass and kf_decode_step on two streams at "
+                         "once, then one merge; cascade-serial: prefix pass, prefix merge, "
+                         "kf_decode_step_merge_partials; cascade-calls: append, prefix pass, suffix decode, merge; "
                          "auto: fused for unsharded workloads with the tensor-core kernel, cascade with a "
                          "shared prefix")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "fp8"],
@@ -762,12 +764,13 @@ def run_ours(args):
                                      and not w.chunk and args.decode_kernel == "tc")
     if w.kv_dtype == "fp8" and args.decode_kernel != "tc":
         raise SystemExit("the FP8 cache is served by the tensor-core kernel only")
-    cascade = bool(w.shared_prefix) and args.path in ("auto", "cascade", "cascade-calls")
+    cascade = bool(w.shared_prefix) and args.path in ("auto", "cascade", "cascade-serial", "cascade-calls")
     chunk = bool(w.chunk)
     if cascade:
         from paged_kv_decode_kf_gb300.step import CascadeStep
         step = CascadeStep(dev, prefix_splits=args.prefix_splits, suffix_splits=args.num_splits,
-                           fused_suffix=args.path != "cascade-calls", out_dtype=out_dtype)
+                           fused_suffix=args.path != "cascade-calls", out_dtype=out_dtype,
+                           concurrent=args.path in ("auto", "cascade"))
         kv_bytes = step.unique_kv_bytes()      # the prefix once, each suffix once
     elif chunk:
         from paged_kv_decode_kf_gb300.step import ChunkStep
@@ -788,9 +791,11 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     # One step with its phases bracketed by events (recorded on the current
-    # stream): fused: [the launch]; cascade with the fused suffix: prefix pass |
-    # prefix merge | suffix step; cascade as calls: append | prefix | suffix |
-    # merge; otherwise append, [attention] | merge.
+    # stream): fused: [the launch]; concurrent cascade, its kernels one after
+    # another so that each is timed alone: prefix pass | suffix step | merge;
+    # cascade with the fused suffix: prefix pass | prefix merge | suffix step;
+    # cascade as calls: append | prefix | suffix | merge; otherwise append,
+    # [attention] | merge.
     def one_step(e):
         if step.fused:
             e[0].record()
@@ -798,6 +803,15 @@ def run_ours(args):
             e[1].record()
             return
         if cascade:
+            if step.concurrent:
+                e[0].record()
+                step.prefix()
+                e[1].record()
+                step.suffix_slot()
+                e[2].record()
+                step.final_merge()
+                e[3].record()
+                return
             if step.fused_suffix:
                 e[0].record()
                 step.prefix()
@@ -857,15 +871,21 @@ def run_ours(args):
     start.record(stream)
     for _ in range(K // g_steps if graph is not None else 0):
         graph.replay()
+    # (a concurrent cascade step runs as it is; its kernels are timed alone
+    # after the region)
+    concurrent = cascade and step.concurrent
     for i in range(K if graph is None else 0):
-        one_step(ev[i])
+        if concurrent:
+            step.run()
+        else:
+            one_step(ev[i])
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
     t1 = time.time()
     ms = start.elapsed_time(end) / K
     phase_source = "events in the timed region (host launches)"
-    if graph is not None and not step.fused:
+    if (graph is not None or concurrent) and not step.fused:
         # the stream first sleeps (a bounded clock spin) while the host enqueues
         # every step, so the events see device time, not host launch gaps
         ev = [events() for _ in range(min(K, 20))]
@@ -875,11 +895,15 @@ def run_ours(args):
             one_step(e)
         torch.cuda.synchronize()
         phase_source = "event-timed pass of %d steps enqueued behind a stream sleep, after the timed region" % len(ev)
+        if concurrent:
+            phase_source += " (the cascade's kernels one after another, each timed alone)"
     elif graph is not None:
         phase_source = "one launch per step: the graph-replayed step time bounds the launch"
     span = lambda k: sum(e[k].elapsed_time(e[k + 1]) for e in ev) / len(ev)
     if cascade:
-        if step.fused_suffix:   # as (append, prefix, suffix, merge): the append is inside the suffix step
+        if step.concurrent:     # as (append, prefix, suffix, merge): the append is inside the suffix step
+            phase_ms = [0.0, span(0), span(1), span(2)]
+        elif step.fused_suffix:
             phase_ms = [0.0, span(0), span(2), span(1)]
         else:
             phase_ms = [span(k) for k in range(4)]
@@ -937,7 +961,7 @@ def run_ours(args):
                 setattr(dev, n, v)
         if cascade:
             step_e = CascadeStep(dev, prefix_splits=step.Sp, suffix_splits=step.Ss, fused_suffix=step.fused_suffix,
-                                 out_dtype=out_dtype)
+                                 out_dtype=out_dtype, concurrent=step.concurrent)
         elif chunk:
             step_e = ChunkStep(dev, num_splits=step.S)
         else:
@@ -1015,7 +1039,11 @@ def run_ours(args):
         pre_s, suf_s = phase_ms[1] * 1e-3, phase_ms[2] * 1e-3
         pre_tf = step.prefix_flops() / pre_s / 1e12
         suf_gbs = step.suffix_kv_bytes() / suf_s / 1e9
-        kernels = {"path": "3 launches: prefix pass, merge of its partials into one, then "
+        kernels = {"path": "3 launches: the prefix pass and kf_decode_step (append + suffix attention + "
+                           "merge of the suffix splits into one slot) on two streams at the same time, then "
+                           "one merge of the prefix slots with the suffix slot; the per-kernel times are "
+                           "each kernel alone, the step overlaps the first two" if step.concurrent else
+                           "3 launches: prefix pass, merge of its partials into one, then "
                            "kf_decode_step_merge_partials (append + suffix attention + merge with the "
                            "prefix partial)" if step.fused_suffix else
                            "4 launches: append, prefix pass, suffix decode, merge",
@@ -1026,7 +1054,12 @@ def run_ours(args):
                                    "peak_source": tsrc + (", of measured" if tsrc.startswith("measured")
                                                           else ", of fallback")},
                    "suffix_decode": {"bound": "hbm", "achieved": suf_gbs, "peak": peak, "unit": "GB/s",
-                                     "frac": suf_gbs / peak, "algorithmic_bytes": step.suffix_kv_bytes()}}
+                                     "frac": suf_gbs / peak, "algorithmic_bytes": step.suffix_kv_bytes()},
+                   # the whole step against its two floors: the unique KV bytes at the HBM
+                   # peak and the prefix FLOPs at the tensor peak
+                   "step": {"us": ms * 1e3, "hbm_floor_us": kv_bytes / (peak * 1e9) * 1e6,
+                            "tensor_floor_us": step.prefix_flops() / (tpk * 1e12) * 1e6,
+                            "frac_of_hbm_floor": kv_bytes / (peak * 1e9) / (ms * 1e-3)}}
         dom = kernels["prefix_pass"] if pre_s >= suf_s else kernels["suffix_decode"]
         roofline_override = dict(dom, traffic=None,
                                  kernel="shared-prefix multi-query pass" if pre_s >= suf_s
@@ -1097,7 +1130,10 @@ def run_ours(args):
                        "step": ("chunk attention (multi-query, causal) + LSE merge" if chunk else
                                 "append + split attention + LSE merge"),
                        "path": "kf_decode_step (one launch)" if step.fused else
-                               ("kf_paged_multiquery_attention (prefix, once) + kf_merge_partials (prefix "
+                               ("kf_paged_multiquery_attention (prefix, once) || kf_decode_step (append + "
+                                "suffixes + their merge, second stream), then kf_merge_partials (prefix slots + "
+                                "suffix slot)" if step.concurrent else
+                                "kf_paged_multiquery_attention (prefix, once) + kf_merge_partials (prefix "
                                 "slots into one) + kf_decode_step_merge_partials (append + suffixes + merge)"
                                 if step.fused_suffix else
                                 "kf_append_kv + kf_paged_multiquery_attention (prefix, once) + "

@@ -121,12 +121,18 @@ class CascadeStep:
     append goes through each request's suffix table; one non-causal
     multi-query pass attends the prefix once for all B queries; decode
     attention covers each request's suffix; one LSE merge combines the two
-    sets of partials. With fused_suffix (the default) that is three launches:
-    the prefix pass, a merge of its slots into one prefix partial, and
-    kf_decode_step_merge_partials (append + suffixes + the final merge)."""
+    sets of partials. With fused_suffix (the default) that is three launches.
+    concurrent (the default): the prefix pass on the caller's stream and
+    kf_decode_step (append + suffixes + the merge of their own splits, one
+    (o, lse) slot per request) on a second stream at the same time -- the
+    first is bound by the tensor pipe, the second by HBM -- then one
+    kf_merge_partials of the prefix pass's slots with the suffix slot. Not
+    concurrent: the prefix pass, a merge of its slots into one prefix partial,
+    and kf_decode_step_merge_partials (append + suffixes + the final merge)."""
 
     def __init__(self, inp: DecodeInputs, prefix_splits: Optional[int] = None,
-                 suffix_splits: Optional[int] = None, out_dtype=torch.float32, fused_suffix: bool = True):
+                 suffix_splits: Optional[int] = None, out_dtype=torch.float32, fused_suffix: bool = True,
+                 concurrent: bool = True):
         w = inp.workload
         assert w.shared_prefix and inp.prefix_table is not None
         self.inp, self.w = inp, w
@@ -151,7 +157,10 @@ class CascadeStep:
         self.Sp, self.Ss = int(prefix_splits), int(suffix_splits)
         self.q_start = torch.tensor([0, B], dtype=torch.int32, device=dev)
         self.prefix_len = torch.tensor([self.P], dtype=torch.int32, device=dev)
-        S = self.Sp + self.Ss
+        self.concurrent = bool(concurrent) and bool(fused_suffix)
+        # slots: the prefix pass's Sp, then the suffix splits (four calls) or
+        # the suffix step's one merged slot (concurrent)
+        S = self.Sp + (1 if self.concurrent else self.Ss)
         self.out_partial = torch.empty((S, B, Hq, w.head_dim), dtype=torch.float32, device=dev)
         self.lse_partial = torch.empty((S, B, Hq), dtype=torch.float32, device=dev)
         self.out = torch.empty((B, Hq, w.head_dim), dtype=out_dtype, device=dev)
@@ -169,6 +178,7 @@ class CascadeStep:
         # step's tail (measured on the cascade workload: 4.5 us vs 8.8 us)
         self.prefix_o = torch.empty((1, B, Hq, w.head_dim), dtype=torch.float32, device=dev)
         self.prefix_lse = torch.empty((1, B, Hq), dtype=torch.float32, device=dev)
+        self.side = torch.cuda.Stream(device=dev) if self.concurrent else None
 
     def append(self, stream=None) -> None:
         i = self.inp
@@ -209,7 +219,34 @@ class CascadeStep:
                                          self.prefix_o, self.prefix_lse, self.workspace,
                                          out=self.out, lse_out=self.lse, stream=stream)
 
+    def suffix_slot(self, stream=None) -> None:
+        """Append, suffix attention and the merge of the suffix splits into the
+        suffix slot (fp32 o and lse after the prefix pass's slots), one launch."""
+        i, w, Sp = self.inp, self.w, self.Sp
+        kf.kf_decode_step(i.q, i.k_new, i.v_new, i.k_cache, i.v_cache, i.suffix_tables, i.suffix_ctx_before,
+                          self.max_suffix, w.scale, self.Ss, self.workspace, out=self.out_partial[Sp],
+                          lse_out=self.lse_partial[Sp], stream=stream)
+
+    def final_merge(self, stream=None) -> None:
+        """The prefix pass's slots and the suffix slot merged into the output."""
+        kf.kf_merge_partials(self.out_partial, self.lse_partial, self.out, lse_out=self.lse, stream=stream)
+
     def run(self, stream=None) -> None:
+        if self.concurrent and (stream is None or isinstance(stream, torch.cuda.Stream)):
+            # fork: the suffix step on the second stream, the prefix pass here;
+            # join before the merge (both are captured as graph branches)
+            main = stream if stream is not None else torch.cuda.current_stream()
+            self.side.wait_stream(main)
+            self.suffix_slot(self.side)
+            self.prefix(main)
+            main.wait_stream(self.side)
+            self.final_merge(main)
+            return
+        if self.concurrent:
+            self.prefix(stream)
+            self.suffix_slot(stream)
+            self.final_merge(stream)
+            return
         if self.fused_suffix:
             self.prefix(stream)
             self.prefix_merge(stream)

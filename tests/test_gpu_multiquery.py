@@ -86,17 +86,18 @@ def test_multiquery_shapes(kf, hq, hkv, d, bs, impl):
     check_partials(o_p.cpu().numpy(), l_p.cpu().numpy(), ref_po, ref_pl, "mq shapes")
 
 
-@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("mode", ["concurrent", "serial", "calls"])
 @pytest.mark.parametrize("impl", IMPLS)
-def test_cascade_prefix_plus_suffix(kf, impl, fused):
+def test_cascade_prefix_plus_suffix(kf, impl, mode):
     """Prefix attended once for all requests, merged with each suffix, equals
-    decode attention over each request's full table -- as two launches
-    (prefix pass + kf_decode_step_merge_partials) or four."""
+    decode attention over each request's full table -- as the prefix pass and
+    the suffix step on two streams then one merge, as three launches in a row
+    (prefix pass, prefix merge, kf_decode_step_merge_partials), or four."""
     from paged_kv_decode_kf_gb300.step import CascadeStep
     w = wl.scaled(wl.CONFIGS["cascade"], batch=6, lengths=wl.Fixed((5, 70, 300, 1, 16, 999)))
     dev = wl.make_inputs(w, "cuda")
     hv_k, hv_v = wl.bf16_bits(dev.k_cache), wl.bf16_bits(dev.v_cache)
-    step = CascadeStep(dev, fused_suffix=fused)
+    step = CascadeStep(dev, fused_suffix=mode != "calls", concurrent=mode == "concurrent")
     with mq_impl(impl):
         step.run()
     torch.cuda.synchronize()

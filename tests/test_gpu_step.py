@@ -159,16 +159,16 @@ def test_bounded_wait_gives_up_cleanly(kf):
     _check_against_oracle(dev, hv, out, lse, what="after a timeout")
 
 
-@pytest.mark.parametrize("kind", ["fused", "balanced", "cascade", "calls"])
+@pytest.mark.parametrize("kind", ["fused", "balanced", "cascade", "cascade_serial", "calls"])
 def test_graph_captured_step_matches_eager(kind):
     """The step's calls need no host synchronisation and allocate nothing, so
     they capture into a CUDA graph (as the benchmark replays them): a replay
     gives the eager step's output and lse bit for bit."""
     from paged_kv_decode_kf_gb300.step import CascadeStep, DecodeStep
-    if kind == "cascade":
+    if kind.startswith("cascade"):
         w = wl.scaled(wl.CONFIGS["cascade"], batch=6, lengths=wl.Fixed((5, 70, 300, 1, 16, 999)))
         dev = wl.make_inputs(w, "cuda")
-        step = CascadeStep(dev)
+        step = CascadeStep(dev, concurrent=kind == "cascade")   # the concurrent form forks a second stream
     else:
         w = wl.scaled(wl.CONFIGS["ragged"], batch=5, lengths=wl.Fixed((500, 31, 2000, 64, 777)))
         dev = wl.make_inputs(w, "cuda")
