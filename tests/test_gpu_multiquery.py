@@ -109,6 +109,29 @@ def test_cascade_prefix_plus_suffix(kf, impl, mode):
     check_lse(step.lse.cpu().numpy(), ref_l, "cascade lse")
 
 
+def test_cascade_concurrent_streams(kf):
+    """The concurrent cascade step forks its suffix step onto a second stream
+    and joins before the merge: run on a caller's non-default stream, on the
+    current stream, or given a raw stream handle (then one stream, in order),
+    it gives the same output and lse bit for bit."""
+    from paged_kv_decode_kf_gb300.step import CascadeStep
+    w = wl.scaled(wl.CONFIGS["cascade"], batch=6, lengths=wl.Fixed((5, 70, 300, 1, 16, 999)))
+    dev = wl.make_inputs(w, "cuda")
+    step = CascadeStep(dev)
+    assert step.concurrent
+    step.run()
+    torch.cuda.synchronize()
+    ref_o, ref_l = step.out.clone(), step.lse.clone()
+    s = torch.cuda.Stream()
+    for how in ("torch stream", "raw handle"):
+        step.out.zero_()
+        step.lse.zero_()
+        s.wait_stream(torch.cuda.current_stream())
+        step.run(s if how == "torch stream" else s.cuda_stream)
+        s.synchronize()
+        assert torch.equal(step.out, ref_o) and torch.equal(step.lse, ref_l), how
+
+
 @pytest.mark.parametrize("impl", IMPLS)
 def test_multiquery_rejects_bad_q_start(kf, impl):
     w, dev, q, qs = _case((40, 50), (3, 3))
